@@ -1,0 +1,239 @@
+/*
+ * ua.h -- C ABI of the unified paged-KV attention forward for GB300 (sm_103a).
+ *
+ * What it computes. For every sequence s of a batch, every query token i of s
+ * and every query head h, the attention output
+ *
+ *     out[cu[s]+i, h, :] = softmax_t(scale * <q[cu[s]+i, h, :], k_t>) v_t
+ *
+ * over the keys t visible to that query, where k_t / v_t are read from a
+ * block-paged cache through the sequence's page table. This is the boxed
+ * O_{t+1} equation of "flashatten takeaways EP2 工程" (kv cache section) with
+ * the tensor layout, page table, GQA grouping and context length of
+ * "vllm_triton_unified_attention_notes" (test_triton_unified_attn,
+ * unified_attention and kernel_unified_attention_2d sections):
+ *
+ *   q            [total_q, num_q_heads, head_dim]                 bf16
+ *   k/v cache    [num_blocks, block_size, num_kv_heads, head_dim] bf16 or fp8 e4m3
+ *                (strides block_size*Hkv*d, Hkv*d, d, 1: all KV heads of one
+ *                 (block, slot) are contiguous)
+ *   out          [total_q, num_q_heads, head_dim]                 bf16
+ *   cu_query_lens[num_seqs+1]  int32, cu[0] = 0, cu[s+1] = cu[s] + q_len(s)
+ *   kv_lens      [num_seqs]    int32, kv_len(s) >= q_len(s); it counts the
+ *                              new query tokens, whose K/V are already cached
+ *   block_tables [num_seqs, max_blocks_per_seq] int32; logical block j of s
+ *                lives in physical block block_tables[s*max_blocks_per_seq+j]
+ *
+ * Visibility: query head h uses KV head h / (Hq/Hkv) (contiguous groups).
+ * Query i of s sits at position pos = kv_len(s) - q_len(s) + i; key t is
+ * visible iff t < kv_len(s), and (causal == 0 or t <= pos), and
+ * (window <= 0 or t > pos - window).
+ *
+ * fp8 e4m3 caches hold per-tensor scaled values: the key is code * k_scale,
+ * the value code * v_scale ("vllm_triton_unified_attention_notes", the load
+ * and quantisation branch). k_scale / v_scale are ignored for bf16 caches.
+ *
+ * Work split. A plan (ua_plan_create) is built on the host from host copies of
+ * the lengths: a CPU scheduler turns (sequence, KV head, row block) programs
+ * into a flat tile list, cutting long key ranges into split-KV pieces whose
+ * partial results are merged by a log-sum-exp combine ("flashatten takeaways
+ * EP2 工程", run_flash_splitkv_fwd and its combine kernel; FlashDecoding in
+ * the "Fused Attention" notes). It replaces the per-program binary search over
+ * the query prefix sums that the vLLM kernel performs at run time.
+ *
+ * Conventions.
+ *  - The caller owns every tensor argument; the plan owns its device tile list,
+ *    per-plan error word and split workspace, and frees them in
+ *    ua_plan_destroy.
+ *  - Device pointers must be 16-byte aligned and tensors contiguous.
+ *  - All device work is ordered on the stream argument; nothing synchronises
+ *    the host except ua_last_device_error and ua_plan_destroy.
+ *  - No entry point calls exit, abort or a device trap. Invalid arguments are
+ *    rejected with a negative status before anything is launched.
+ */
+#ifndef UA_H
+#define UA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-identical to cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* ua_stream_t;
+
+typedef enum {
+  UA_OK = 0,
+  UA_ERR_INVALID_ARG = -1,   /* bad size, length, pointer or alignment */
+  UA_ERR_UNSUPPORTED = -2,   /* valid but not built: head_dim, dtype, block_size */
+  UA_ERR_CUDA = -3,          /* a CUDA runtime/driver call failed */
+  UA_ERR_WORKSPACE = -4,     /* workspace missing or too small */
+  UA_ERR_DEVICE_TIMEOUT = -5,/* a bounded device-side wait gave up (error word) */
+  UA_ERR_BOUNDS = -6         /* a page id outside [0, num_blocks) was met (error word) */
+} ua_status;
+
+typedef enum { UA_KV_BF16 = 0, UA_KV_FP8_E4M3 = 1 } ua_kv_dtype;
+
+/* One unit of scheduled work, 8 x int32 (32 bytes), shared by the prefill
+ * and decode lists. Rows are the packed (token, head) pairs of one KV head:
+ * row r of sequence s and KV head g is query token r / qpk and query head
+ * g * qpk + r % qpk, qpk = Hq / Hkv (the packed GQA tile of the vLLM kernel). */
+typedef struct {
+  int32_t seq;      /* sequence index */
+  int32_t kv_head;  /* KV head g */
+  int32_t row0;     /* first packed row of this tile */
+  int32_t nrows;    /* rows in this tile (<= 8 decode, <= 128 prefill) */
+  int32_t kv_lo;    /* first key position this tile reads */
+  int32_t kv_hi;    /* one past the last key position this tile reads */
+  int32_t slot;     /* split workspace slot, or -1: write the output directly */
+  int32_t group;    /* combine group of the split, or -1 */
+} ua_tile;
+
+/* A combine group: the consecutive workspace slots holding the split partials
+ * of one (sequence, KV head, row block). */
+typedef struct {
+  int32_t seq, kv_head, row0, nrows;
+  int32_t slot0;    /* first slot */
+  int32_t nsplits;  /* number of consecutive slots, 2..UA_MAX_SPLITS */
+  int32_t pad0, pad1;
+} ua_combine_group;
+
+#define UA_MAX_SPLITS 128
+#define UA_DECODE_ROWS 8     /* rows of one decode tile */
+#define UA_PREFILL_ROWS 128  /* rows of one prefill tile (tcgen05 M) */
+
+typedef struct {
+  int64_t num_prefill_tiles;
+  int64_t num_decode_tiles;    /* includes every split piece */
+  int64_t num_combine_groups;
+  int64_t num_slots;           /* split workspace slots */
+  int64_t workspace_bytes;     /* bytes of split workspace the plan owns */
+  int32_t split_tokens;        /* key tokens per split piece (0: no splits) */
+  int32_t num_sms;             /* SM count the schedule was sized for */
+} ua_plan_info;
+
+typedef struct ua_plan ua_plan;
+
+/*
+ * ua_schedule -- the CPU scheduler alone: host memory only, no CUDA call.
+ * Validates the problem and writes the tile lists the plan would upload.
+ * Call once with NULL arrays to read the counts into *info, then again with
+ * arrays of at least those lengths (the *_cap arguments give their lengths in
+ * elements; too small a capacity returns UA_ERR_INVALID_ARG).
+ * num_splits: 0 = automatic (enough pieces for num_sms), n > 0 = cut every
+ * decode tile's key range into min(n, ceil(len/16)) pieces; at most
+ * UA_MAX_SPLITS. num_sms <= 0 means 152.
+ * decode_rows_max: sequences with q_len * qpk <= this value go to the decode
+ * kernel, the others to the prefill kernel; < 0 means the built-in default.
+ */
+ua_status ua_schedule(const int32_t* cu_query_lens_host, const int32_t* kv_lens_host,
+                      int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                      int32_t kv_dtype, int32_t causal, int32_t window, int32_t num_splits,
+                      int32_t num_sms, int32_t decode_rows_max, ua_plan_info* info,
+                      ua_tile* prefill_tiles, int64_t prefill_cap,
+                      ua_tile* decode_tiles, int64_t decode_cap,
+                      ua_combine_group* groups, int64_t groups_cap);
+
+/*
+ * ua_plan_create -- run the scheduler for the current CUDA device and upload
+ * the tile lists with one stream-ordered copy; allocates the plan's device
+ * memory (tile lists, error word, split workspace).
+ * Arguments as ua_schedule; num_sms is queried from the device.
+ * Returns UA_ERR_INVALID_ARG / UA_ERR_UNSUPPORTED for a rejected problem,
+ * UA_ERR_CUDA when an allocation or copy fails (nothing is leaked).
+ */
+ua_status ua_plan_create(ua_plan** out, const int32_t* cu_query_lens_host,
+                         const int32_t* kv_lens_host, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t max_blocks_per_seq, int32_t kv_dtype, int32_t causal,
+                         int32_t window, int32_t num_splits, ua_stream_t stream);
+
+/* Same with an explicit decode/prefill row threshold (see ua_schedule). */
+ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
+                            const int32_t* kv_lens_host, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t max_blocks_per_seq, int32_t kv_dtype, int32_t causal,
+                            int32_t window, int32_t num_splits, int32_t decode_rows_max,
+                            ua_stream_t stream);
+
+/*
+ * ua_forward -- attention for the batch the plan was built for.
+ * q, k_cache, v_cache, out: device tensors in the layouts above.
+ * cu_query_lens, kv_lens, block_tables: device copies. cu_query_lens and
+ * kv_lens must hold the values given to the plan; the kernels read them for
+ * each tile's query offset and masking and clamp every key range by
+ * kv_lens[seq], and the page index by max_blocks_per_seq.
+ * num_blocks: physical blocks in each cache; a page id outside
+ * [0, num_blocks) is never dereferenced: the page is treated as masked and
+ * UA_ERR_BOUNDS is recorded in the plan's error word.
+ * max_q / max_kv: the largest q_len / kv_len (checked against the plan).
+ * scale: multiplies q.k as given (not assumed to be 1/sqrt(d)).
+ * Launches the prefill kernel, the decode kernel and, if any tile was split,
+ * the combine kernel on `stream`. Not thread-safe per plan: calls that share
+ * a plan must be ordered (they share its split workspace).
+ */
+ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
+                     const void* v_cache, void* out, const int32_t* cu_query_lens,
+                     const int32_t* kv_lens, const int32_t* block_tables, int64_t num_blocks,
+                     int32_t max_q, int32_t max_kv, float scale, float k_scale, float v_scale,
+                     ua_stream_t stream);
+
+/*
+ * ua_forward_oneshot -- the whole call in one: host copies of the lengths
+ * (for the scheduler) plus the device tensors; builds a transient plan,
+ * runs ua_forward, and frees the plan after the stream has drained it.
+ * Synchronises `stream` before returning.
+ */
+ua_status ua_forward_oneshot(const void* q, const void* k_cache, const void* v_cache, void* out,
+                             const int32_t* cu_query_lens_host, const int32_t* kv_lens_host,
+                             const int32_t* cu_query_lens, const int32_t* kv_lens,
+                             const int32_t* block_tables, int32_t num_seqs,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t max_blocks_per_seq,
+                             int64_t num_blocks, int32_t kv_dtype, int32_t max_q,
+                             int32_t max_kv, float scale, int32_t causal, int32_t window,
+                             float k_scale, float v_scale, int32_t num_splits,
+                             ua_stream_t stream);
+
+/* Counts and sizes of a plan (host memory only). */
+ua_status ua_plan_get_info(const ua_plan* plan, ua_plan_info* info);
+
+/* Kernel timing for measurement tools. While enabled, ua_forward records a
+ * CUDA event pair on its stream around each kernel launch (negligible cost);
+ * ua_plan_kernel_times synchronises, sums the elapsed milliseconds and launch
+ * counts per kernel kind since the last read -- index 0 prefill, 1 decode,
+ * 2 combine -- into ms[0..2] / launches[0..2], and clears them. */
+ua_status ua_plan_set_profiling(ua_plan* plan, int32_t enable);
+ua_status ua_plan_kernel_times(ua_plan* plan, float* ms, int64_t* launches);
+
+/* Synchronises the plan's last stream, reads the device error word
+ * (UA_OK, UA_ERR_BOUNDS or UA_ERR_DEVICE_TIMEOUT) into *code and clears it. */
+ua_status ua_last_device_error(ua_plan* plan, int32_t* code);
+
+ua_status ua_plan_destroy(ua_plan* plan);
+
+/* Static string for a status code (never NULL). */
+const char* ua_status_string(int32_t status);
+
+/*
+ * ua_gather_kv_debug -- test aid for bit-exact index checks. For every decode
+ * tile of the plan, in order, copies the raw K and V rows of its key range
+ * [kv_lo, kv_hi) (clamped by kv_lens[seq]) for its KV head into k_out/v_out,
+ * packed tile after tile, rows of head_dim elements of the cache's element
+ * size. The row offset of tile n is the sum of the clamped range lengths of
+ * tiles 0..n-1. Page ids are resolved exactly as in ua_forward. The outputs
+ * must hold `rows_cap` rows.
+ */
+ua_status ua_gather_kv_debug(const ua_plan* plan, const void* k_cache, const void* v_cache,
+                             const int32_t* kv_lens, const int32_t* block_tables,
+                             int64_t num_blocks, void* k_out, void* v_out, int64_t rows_cap,
+                             ua_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UA_H */

@@ -1,0 +1,459 @@
+// Split-KV decode kernel (K-D): a bandwidth-bound pass over the paged cache.
+//
+// Work unit: one ua_tile = up to 8 packed (token, head) rows of one sequence
+// and KV head (all query heads of a GQA group share one K/V stream, as in the
+// packed Q tile of "vllm_triton_unified_attention_notes") over one key range
+// [kv_lo, kv_hi) -- a whole range, or one split piece whose partial result is
+// merged later by the log-sum-exp combine (FlashDecoding, "Fused Attention"
+// notes; run_flash_splitkv_fwd in "flashatten takeaways EP2 工程").
+//
+// Design for sm_103a. Decode is HBM-bound (about 4-16 flop per cache byte),
+// so the kernel streams K/V pages straight from HBM into registers with
+// 16-byte read-only loads, one step (16 keys) ahead of the math, and keeps
+// the math on the tensor pipe with m16n8k16 MMAs in a transposed orientation:
+//   S^T[key, row]  = K[key, :] . Q[row, :]      (M = 16 keys, N = 8 rows)
+//   O^T[d, row]   += V^T[d, key] . P^T[key, row] (M = 16 dims, N = 8 rows)
+// Keys on M and the GQA rows on N waste no MMA rows when 8 query heads share
+// a KV head. The score fragment becomes the PV operand with one movmatrix
+// transpose per 8x8 block. Because the contraction index of both products
+// and the M index of the second may be permuted freely, the kernel assigns
+// keys and head dimensions to lanes so that every 16-byte load is fully
+// coalesced (4 lanes x 16 B of one K row, 8 lanes x 16 B of one V row).
+// Online softmax in base 2 ("Fused Attention" notes, _attn_fwd_inner): running
+// max m, running sum l, rescale factor 2^(m_old - m_new).
+// Four warps per CTA take interleaved 16-key steps of the tile's range and
+// merge their (m, l, O) through shared memory at the end.
+#include "ua_device.cuh"
+#include "ua_kernels.h"
+
+namespace ua {
+
+namespace {
+
+template <int D, bool FP8>
+struct DecodeCfg {
+  static constexpr int ELT = FP8 ? 1 : 2;                       // cache element bytes
+  static constexpr int KE = (16 / ELT) < (D / 4) ? (16 / ELT) : (D / 4);  // K values per load
+  static constexpr int KVALS = D / 4;                           // K values per row per lane
+  static constexpr int KW = KVALS * ELT / 4;                    // ... as 32-bit words
+  static constexpr int NKL = KVALS / KE;                        // K loads per row
+  static constexpr int VE = (16 / ELT) < (D / 8) ? (16 / ELT) : (D / 8);  // V values per load
+  static constexpr int VVALS = D / 8;                           // V values per key per lane
+  static constexpr int VW = VVALS * ELT / 4;
+  static constexpr int NVL = VVALS / VE;
+  static constexpr int VLB = VE * ELT;                          // bytes per V load (16 or 8)
+  static constexpr int NC = D / 16;                             // MMA chunks along D
+  static constexpr int QW = KVALS / 2;                          // Q words (16-bit pairs)
+};
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+
+// Key slot (0..15) of a step held as MMA row m of S^T. Chosen so that the
+// PV contraction slots 2t, 2t+1, 2t+8, 2t+9 of lane t are keys 4t..4t+3.
+__device__ __forceinline__ int key_of_row(int m) {
+  return (m < 8) ? ((m & 1) ? 2 * m - 1 : 2 * m) : ((m & 1) ? 2 * m - 15 : 2 * m - 14);
+}
+
+// Head-dimension index of K/Q value u (0..D/4-1) of lane t.
+template <int D, bool FP8>
+__device__ __forceinline__ int k_dim(int u, int t) {
+  using C = DecodeCfg<D, FP8>;
+  return (u / C::KE) * 4 * C::KE + t * C::KE + (u % C::KE);
+}
+
+// Head-dimension index of V value v (0..D/8-1) of lane group g.
+template <int D, bool FP8>
+__device__ __forceinline__ int v_dim(int v, int g) {
+  using C = DecodeCfg<D, FP8>;
+  return (v / C::VE) * 8 * C::VE + g * C::VE + (v % C::VE);
+}
+
+template <int D, bool FP8>
+struct StepRegs {
+  uint32_t k[2][DecodeCfg<D, FP8>::KW];   // K rows key_of_row(g), key_of_row(g+8)
+  uint32_t v[4][DecodeCfg<D, FP8>::VW];   // V rows 4t .. 4t+3
+};
+
+// Issue the loads of one 16-key step starting at key `base` of page `page`
+// (-1: nothing readable). Keys at or beyond kv_hi read as zero.
+template <int D, bool FP8>
+__device__ __forceinline__ void load_step(StepRegs<D, FP8>& r, const KernelParams& p,
+                                          const uint8_t* kc, const uint8_t* vc, int base,
+                                          int64_t page, int kv_hi, int kv_head, int g, int t) {
+  using C = DecodeCfg<D, FP8>;
+  const int slot0 = base % p.block_size;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int key = key_of_row(g + 8 * h);
+    const bool ok = page >= 0 && base + key < kv_hi;
+    const uint8_t* row =
+        kc + (kv_row_offset(p, page < 0 ? 0 : page, slot0 + key, kv_head, D)) * C::ELT;
+#pragma unroll
+    for (int l = 0; l < C::NKL; ++l) {
+      uint4 x = make_uint4(0u, 0u, 0u, 0u);
+      if (ok) x = ld_stream_v4(row + (l * 4 * C::KE + t * C::KE) * C::ELT);
+      r.k[h][4 * l + 0] = x.x;
+      r.k[h][4 * l + 1] = x.y;
+      r.k[h][4 * l + 2] = x.z;
+      r.k[h][4 * l + 3] = x.w;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int key = 4 * t + j;
+    const bool ok = page >= 0 && base + key < kv_hi;
+    const uint8_t* row =
+        vc + (kv_row_offset(p, page < 0 ? 0 : page, slot0 + key, kv_head, D)) * C::ELT;
+#pragma unroll
+    for (int l = 0; l < C::NVL; ++l) {
+      const uint8_t* a = row + (l * 8 * C::VE + g * C::VE) * C::ELT;
+      if constexpr (C::VLB == 16) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (ok) x = ld_stream_v4(a);
+        r.v[j][4 * l + 0] = x.x;
+        r.v[j][4 * l + 1] = x.y;
+        r.v[j][4 * l + 2] = x.z;
+        r.v[j][4 * l + 3] = x.w;
+      } else {
+        uint2 x = make_uint2(0u, 0u);
+        if (ok) x = ld_stream_v2(a);
+        r.v[j][2 * l + 0] = x.x;
+        r.v[j][2 * l + 1] = x.y;
+      }
+    }
+  }
+}
+
+// Per-warp online-softmax state for the two rows (columns n = 2t, 2t+1) a lane
+// holds, plus its O^T accumulator fragments.
+template <int D>
+struct WarpState {
+  float acc[D / 16][4];
+  float m[2];
+  float l[2];  // lane-partial sums; reduced over the 8 lane groups at the end
+};
+
+struct StepMask {
+  int kv_hi;       // keys >= kv_hi are outside the range
+  int hi_full;     // keys < hi_full are visible to every row (upper side)
+  int lo_full;     // keys >= lo_full are visible to every row (lower side)
+  int pos[2];      // query position of the lane's two rows
+  int causal;
+  int window;
+};
+
+template <int D, bool FP8>
+__device__ __forceinline__ void compute_step(WarpState<D>& st, const StepRegs<D, FP8>& r,
+                                             const uint32_t (&qb)[D / 16][2], const float (&cc)[2],
+                                             const StepMask& mk, int base, int g, int t) {
+  using C = DecodeCfg<D, FP8>;
+  // S^T = K Q^T for the 16 keys of this step.
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < C::NC; ++c) {
+    uint32_t a[4];
+    if constexpr (FP8) {
+      a[0] = e4m3x2_to_f16x2(r.k[0][c]);
+      a[1] = e4m3x2_to_f16x2(r.k[1][c]);
+      a[2] = e4m3x2_to_f16x2(r.k[0][c] >> 16);
+      a[3] = e4m3x2_to_f16x2(r.k[1][c] >> 16);
+    } else {
+      a[0] = r.k[0][2 * c];
+      a[1] = r.k[1][2 * c];
+      a[2] = r.k[0][2 * c + 1];
+      a[3] = r.k[1][2 * c + 1];
+    }
+    mma16816<FP8>(s, a, qb[c][0], qb[c][1]);
+  }
+  float x[4];
+  x[0] = s[0] * cc[0];
+  x[1] = s[1] * cc[1];
+  x[2] = s[2] * cc[0];
+  x[3] = s[3] * cc[1];
+  // Masking (a select, so that nothing read from outside the visible set can
+  // reach the result) only on steps that straddle a bound.
+  if (base < mk.lo_full || base + 16 > mk.hi_full) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int key = base + key_of_row(g + 8 * (e >> 1));
+      const int pos = mk.pos[e & 1];
+      bool ok = key < mk.kv_hi;
+      if (mk.causal) ok = ok && key <= pos;
+      if (mk.window > 0) ok = ok && key > pos - mk.window;
+      x[e] = ok ? x[e] : -INFINITY;
+    }
+  }
+  // Row max over the 16 keys: the lane's two keys, then the 8 lane groups.
+  float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 4));
+    mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
+    mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
+  }
+  float p[4];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float m_new = fmaxf(st.m[j], mx[j]);
+    // Rows with nothing visible yet keep m = -inf; subtract 0 instead so that
+    // no -inf - -inf appears.
+    const float sub = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = ex2(st.m[j] - sub);
+    p[j] = ex2(x[j] - sub);
+    p[j + 2] = ex2(x[j + 2] - sub);
+    st.l[j] = st.l[j] * alpha + p[j] + p[j + 2];
+    st.m[j] = m_new;
+#pragma unroll
+    for (int c = 0; c < C::NC; ++c) {
+      st.acc[c][j] *= alpha;
+      st.acc[c][j + 2] *= alpha;
+    }
+  }
+  // P^T as the B operand of the PV product: transpose the two 8x8 blocks.
+  const uint32_t pb0 = movmatrix_trans(pack2<FP8>(p[0], p[1]));
+  const uint32_t pb1 = movmatrix_trans(pack2<FP8>(p[2], p[3]));
+  // O^T += V^T P^T.
+#pragma unroll
+  for (int c = 0; c < C::NC; ++c) {
+    uint32_t a[4];
+    if constexpr (FP8) {
+      const uint32_t sel = (c & 1) ? 0x7362u : 0x5140u;
+      const uint32_t lo = __byte_perm(r.v[0][c >> 1], r.v[1][c >> 1], sel);
+      const uint32_t hi = __byte_perm(r.v[2][c >> 1], r.v[3][c >> 1], sel);
+      a[0] = e4m3x2_to_f16x2(lo);
+      a[1] = e4m3x2_to_f16x2(lo >> 16);
+      a[2] = e4m3x2_to_f16x2(hi);
+      a[3] = e4m3x2_to_f16x2(hi >> 16);
+    } else {
+      a[0] = __byte_perm(r.v[0][c], r.v[1][c], 0x5410u);
+      a[1] = __byte_perm(r.v[0][c], r.v[1][c], 0x7632u);
+      a[2] = __byte_perm(r.v[2][c], r.v[3][c], 0x5410u);
+      a[3] = __byte_perm(r.v[2][c], r.v[3][c], 0x7632u);
+    }
+    mma16816<FP8>(st.acc[c], a, pb0, pb1);
+  }
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kThreads)
+    decode_kernel(const KernelParams p) {
+  using C = DecodeCfg<D, FP8>;
+  __shared__ float red_acc[kWarps][UA_DECODE_ROWS][D];
+  __shared__ float red_m[kWarps][UA_DECODE_ROWS];
+  __shared__ float red_l[kWarps][UA_DECODE_ROWS];
+
+  const ua_tile tile = p.tiles[blockIdx.x];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+
+  // Per-sequence values from the device arrays; every range is clamped so
+  // that disagreeing host/device lengths cannot send a read out of bounds.
+  const int q_start = p.cu_query_lens[tile.seq];
+  const int qlen = p.cu_query_lens[tile.seq + 1] - q_start;
+  const int kv_len = p.kv_lens[tile.seq];
+  const int ctx = kv_len - qlen;
+  const int nrows = min(tile.nrows, qlen * p.qpk - tile.row0);
+  const int kv_hi = min(min(tile.kv_hi, kv_len), p.max_blocks_per_seq * p.block_size);
+  const int kv_lo = tile.kv_lo;
+
+  // ---- Q fragments (B operand of S^T = K Q^T): row n = g of the tile.
+  uint32_t qb[C::NC][2];
+  float cc[2];
+  {
+    uint32_t qw[C::QW];
+    const bool row_ok = g < nrows;
+    const int r = tile.row0 + (row_ok ? g : 0);
+    const int tok = q_start + r / p.qpk;
+    const int head = tile.kv_head * p.qpk + r % p.qpk;
+    const uint8_t* qrow = reinterpret_cast<const uint8_t*>(p.q) +
+                          (static_cast<int64_t>(tok) * p.num_q_heads + head) * D * 2;
+#pragma unroll
+    for (int l = 0; l < C::NKL; ++l) {
+#pragma unroll
+      for (int h = 0; h < C::KE / 8; ++h) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (row_ok) x = *reinterpret_cast<const uint4*>(qrow + (l * 4 * C::KE + t * C::KE + 8 * h) * 2);
+        const int w = l * (C::KE / 2) + 4 * h;
+        qw[w + 0] = x.x;
+        qw[w + 1] = x.y;
+        qw[w + 2] = x.z;
+        qw[w + 3] = x.w;
+      }
+    }
+    if constexpr (FP8) {
+      // f16 operands for the e4m3 path: scale each Q row by a power of two so
+      // that its largest magnitude lies in [2^14, 2^15); exact for every
+      // element within 2^-29 of the row maximum. The factor is undone in the
+      // per-row score multiplier.
+      float amax = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::QW; ++w) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[w]));
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      int e = 0;
+      if (amax > 0.f && amax < INFINITY) {
+        int E;
+        frexpf(amax, &E);
+        e = min(max(15 - E, -126), 126);
+      }
+      const float up = __int_as_float((127 + e) << 23);
+      const float down = __int_as_float((127 - e) << 23);
+#pragma unroll
+      for (int w = 0; w < C::QW; ++w) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&qw[w]));
+        qw[w] = pack2<true>(f.x * up, f.y * up);
+      }
+      const float row_mult = p.score_scale_log2 * down;
+      cc[0] = __shfl_sync(0xffffffffu, row_mult, 4 * (2 * t));
+      cc[1] = __shfl_sync(0xffffffffu, row_mult, 4 * (2 * t + 1));
+    } else {
+      cc[0] = cc[1] = p.score_scale_log2;
+    }
+#pragma unroll
+    for (int c = 0; c < C::NC; ++c) {
+      qb[c][0] = qw[2 * c];
+      qb[c][1] = qw[2 * c + 1];
+    }
+  }
+
+  // ---- Visibility of the lane's two rows (columns n = 2t, 2t+1).
+  StepMask mk;
+  mk.kv_hi = kv_hi;
+  mk.causal = p.causal;
+  mk.window = p.window;
+  {
+    const int last = max(nrows - 1, 0);
+    const int min_pos = ctx + tile.row0 / p.qpk;
+    const int max_pos = ctx + (tile.row0 + last) / p.qpk;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int n = 2 * t + j;
+      mk.pos[j] = (n < nrows) ? ctx + (tile.row0 + n) / p.qpk : max_pos;
+    }
+    mk.hi_full = p.causal ? min(kv_hi, min_pos + 1) : kv_hi;
+    mk.lo_full = p.window > 0 ? max_pos - p.window + 1 : INT_MIN;
+  }
+
+  WarpState<D> st;
+#pragma unroll
+  for (int c = 0; c < C::NC; ++c)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) st.acc[c][e] = 0.f;
+  st.m[0] = st.m[1] = -INFINITY;
+  st.l[0] = st.l[1] = 0.f;
+
+  // ---- Stream the key range: warp w takes steps w, w+4, w+8, ...
+  const uint8_t* kc = reinterpret_cast<const uint8_t*>(p.k_cache);
+  const uint8_t* vc = reinterpret_cast<const uint8_t*>(p.v_cache);
+  const int nsteps = kv_hi > kv_lo ? (kv_hi - kv_lo + 15) / 16 : 0;
+  const int my_n = nsteps > warp ? (nsteps - warp + kWarps - 1) / kWarps : 0;
+  auto step_base = [&](int k) { return kv_lo + 16 * (warp + kWarps * k); };
+
+  StepRegs<D, FP8> ra, rb;
+  if (my_n > 0) {
+    int64_t pg_next = my_n > 1 ? page_of(p, tile.seq, step_base(1)) : -1;
+    load_step<D, FP8>(ra, p, kc, vc, step_base(0), page_of(p, tile.seq, step_base(0)), kv_hi,
+                      tile.kv_head, g, t);
+    for (int k = 0; k < my_n; k += 2) {
+      if (k + 1 < my_n)
+        load_step<D, FP8>(rb, p, kc, vc, step_base(k + 1), pg_next, kv_hi, tile.kv_head, g, t);
+      int64_t pg_n2 = k + 2 < my_n ? page_of(p, tile.seq, step_base(k + 2)) : -1;
+      compute_step<D, FP8>(st, ra, qb, cc, mk, step_base(k), g, t);
+      if (k + 1 >= my_n) break;
+      if (k + 2 < my_n)
+        load_step<D, FP8>(ra, p, kc, vc, step_base(k + 2), pg_n2, kv_hi, tile.kv_head, g, t);
+      pg_next = k + 3 < my_n ? page_of(p, tile.seq, step_base(k + 3)) : -1;
+      compute_step<D, FP8>(st, rb, qb, cc, mk, step_base(k + 1), g, t);
+    }
+  }
+
+  // ---- Merge the four warps.
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 4);
+    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 8);
+    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 16);
+  }
+  if (g == 0) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      red_m[warp][2 * t + j] = st.m[j];
+      red_l[warp][2 * t + j] = st.l[j];
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < C::NC; ++c) {
+    const int d0 = v_dim<D, FP8>(2 * c, g);
+    red_acc[warp][2 * t][d0] = st.acc[c][0];
+    red_acc[warp][2 * t + 1][d0] = st.acc[c][1];
+    red_acc[warp][2 * t][d0 + 1] = st.acc[c][2];
+    red_acc[warp][2 * t + 1][d0 + 1] = st.acc[c][3];
+  }
+  __syncthreads();
+
+  constexpr int kSeg = D / 16;  // dims per thread in the epilogue
+  const int n = threadIdx.x / 16;
+  const int d0 = (threadIdx.x % 16) * kSeg;
+  if (n >= nrows) return;
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][n]);
+  float L = 0.f;
+  float o[kSeg];
+#pragma unroll
+  for (int e = 0; e < kSeg; ++e) o[e] = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const float mw = red_m[w][n];
+    const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+    L += f * red_l[w][n];
+#pragma unroll
+    for (int e = 0; e < kSeg; ++e) o[e] += f * red_acc[w][n][d0 + e];
+  }
+  const float inv = L > 0.f ? p.v_scale / L : 0.f;
+  if (tile.slot < 0) {
+    const int r = tile.row0 + n;
+    const int tok = q_start + r / p.qpk;
+    const int head = tile.kv_head * p.qpk + r % p.qpk;
+    uint32_t packed[kSeg / 2];
+#pragma unroll
+    for (int e = 0; e < kSeg / 2; ++e) packed[e] = pack2<false>(o[2 * e] * inv, o[2 * e + 1] * inv);
+    uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) +
+                   ((static_cast<int64_t>(tok) * p.num_q_heads + head) * D + d0) * 2;
+    if constexpr (kSeg == 8) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    } else {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+    }
+  } else {
+    float* wo = p.ws_o + (static_cast<int64_t>(tile.slot) * UA_DECODE_ROWS + n) * D + d0;
+#pragma unroll
+    for (int e = 0; e < kSeg; e += 4)
+      *reinterpret_cast<float4*>(wo + e) =
+          make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+    if (threadIdx.x % 16 == 0)
+      p.ws_lse[static_cast<int64_t>(tile.slot) * UA_DECODE_ROWS + n] =
+          L > 0.f ? M + log2f(L) : -INFINITY;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cudaStream_t stream) {
+  if (p.num_tiles <= 0) return cudaSuccess;
+  const dim3 grid(p.num_tiles), block(kThreads);
+  if (kv_dtype == UA_KV_BF16) {
+    if (head_dim == 128) decode_kernel<128, false><<<grid, block, 0, stream>>>(p);
+    else decode_kernel<64, false><<<grid, block, 0, stream>>>(p);
+  } else {
+    if (head_dim == 128) decode_kernel<128, true><<<grid, block, 0, stream>>>(p);
+    else decode_kernel<64, true><<<grid, block, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ua

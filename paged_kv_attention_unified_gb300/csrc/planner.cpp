@@ -1,0 +1,174 @@
+// Host-side work scheduler (see planner.h).
+#include "planner.h"
+
+#include <algorithm>
+#include <climits>
+
+namespace ua {
+
+namespace {
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+inline int64_t round_down(int64_t a, int64_t b) { return (a / b) * b; }
+
+// Key range [lo, hi) read by the packed rows [row0, row0 + nrows) of one
+// sequence. Query token i = row / qpk sits at pos = ctx + i; with a causal
+// mask it sees keys up to pos, with a window only keys above pos - window.
+// lo is rounded down to the 16-token step; the kernels mask what lies below
+// the true bound.
+void key_range(const Problem& p, int32_t ctx, int32_t kv_len, int32_t row0, int32_t nrows,
+               int32_t* lo, int32_t* hi) {
+  const int qpk = p.num_q_heads / p.num_kv_heads;
+  const int64_t min_pos = ctx + row0 / qpk;
+  const int64_t max_pos = ctx + (row0 + nrows - 1) / qpk;
+  int64_t h = p.causal ? std::min<int64_t>(kv_len, max_pos + 1) : kv_len;
+  int64_t l = 0;
+  if (p.window > 0) l = std::max<int64_t>(0, min_pos - p.window + 1);
+  l = round_down(l, kKeyStep);
+  if (h < l) h = l;
+  *lo = static_cast<int32_t>(l);
+  *hi = static_cast<int32_t>(h);
+}
+
+}  // namespace
+
+ua_status validate(const Problem& p) {
+  if (p.num_seqs < 0 || p.num_q_heads <= 0 || p.num_kv_heads <= 0 || p.head_dim <= 0 ||
+      p.block_size <= 0 || p.max_blocks_per_seq < 0)
+    return UA_ERR_INVALID_ARG;
+  if (p.num_q_heads % p.num_kv_heads != 0) return UA_ERR_INVALID_ARG;
+  if (p.kv_dtype != UA_KV_BF16 && p.kv_dtype != UA_KV_FP8_E4M3) return UA_ERR_INVALID_ARG;
+  if (p.num_splits < 0 || p.num_splits > UA_MAX_SPLITS) return UA_ERR_INVALID_ARG;
+  if (p.causal != 0 && p.causal != 1) return UA_ERR_INVALID_ARG;
+  if (p.num_seqs > 0 && (p.cu_query_lens == nullptr || p.kv_lens == nullptr))
+    return UA_ERR_INVALID_ARG;
+  if (p.head_dim != 64 && p.head_dim != 128) return UA_ERR_UNSUPPORTED;
+  if (p.block_size % kKeyStep != 0) return UA_ERR_UNSUPPORTED;
+  if (p.num_seqs == 0) return UA_OK;
+  if (p.cu_query_lens[0] != 0) return UA_ERR_INVALID_ARG;
+  const int64_t qpk = p.num_q_heads / p.num_kv_heads;
+  for (int s = 0; s < p.num_seqs; ++s) {
+    const int64_t q0 = p.cu_query_lens[s], q1 = p.cu_query_lens[s + 1];
+    const int64_t ql = q1 - q0, kv = p.kv_lens[s];
+    if (ql < 0 || kv < 0 || kv < ql) return UA_ERR_INVALID_ARG;
+    if (ceil_div(kv, p.block_size) > p.max_blocks_per_seq) return UA_ERR_INVALID_ARG;
+    if (ql * qpk > INT32_MAX) return UA_ERR_INVALID_ARG;
+  }
+  // key positions must fit the page table in int32 arithmetic
+  if (static_cast<int64_t>(p.max_blocks_per_seq) * p.block_size > INT32_MAX)
+    return UA_ERR_INVALID_ARG;
+  return UA_OK;
+}
+
+ua_status build_schedule(const Problem& p, Schedule* out) {
+  ua_status st = validate(p);
+  if (st != UA_OK) return st;
+  Schedule s;
+  const int qpk = p.num_q_heads / p.num_kv_heads;
+  const int64_t rows_max = p.decode_rows_max < 0 ? kDefaultDecodeRowsMax : p.decode_rows_max;
+  const int num_sms = p.num_sms > 0 ? p.num_sms : 152;
+
+  // 1. Whole decode tiles (before splitting) and prefill tiles.
+  std::vector<ua_tile> dec;
+  for (int32_t q = 0; q < p.num_seqs; ++q) {
+    const int32_t ql = p.cu_query_lens[q + 1] - p.cu_query_lens[q];
+    const int32_t kv = p.kv_lens[q];
+    s.max_q = std::max(s.max_q, ql);
+    s.max_kv = std::max(s.max_kv, kv);
+    if (ql == 0) continue;
+    const int32_t ctx = kv - ql;
+    const int64_t rows = static_cast<int64_t>(ql) * qpk;
+    const bool is_decode = rows <= rows_max;
+    const int step = is_decode ? UA_DECODE_ROWS : UA_PREFILL_ROWS;
+    for (int32_t g = 0; g < p.num_kv_heads; ++g) {
+      for (int64_t r0 = 0; r0 < rows; r0 += step) {
+        ua_tile t;
+        t.seq = q;
+        t.kv_head = g;
+        t.row0 = static_cast<int32_t>(r0);
+        t.nrows = static_cast<int32_t>(std::min<int64_t>(step, rows - r0));
+        key_range(p, ctx, kv, t.row0, t.nrows, &t.kv_lo, &t.kv_hi);
+        t.slot = -1;
+        t.group = -1;
+        (is_decode ? dec : s.prefill).push_back(t);
+      }
+    }
+  }
+
+  // 2. Split-KV for decode tiles (FlashDecoding): one chunk length C for the
+  // whole batch, so that pieces are equal-sized and load-balance well.
+  int64_t total = 0, longest = 0;
+  for (const ua_tile& t : dec) {
+    total += t.kv_hi - t.kv_lo;
+    longest = std::max<int64_t>(longest, t.kv_hi - t.kv_lo);
+  }
+  int64_t chunk = 0;  // 0: do not split
+  if (p.num_splits == 0 && !dec.empty()) {
+    const int64_t target = static_cast<int64_t>(num_sms) * kDecodeCtasPerSm * kDecodeWaves;
+    if (static_cast<int64_t>(dec.size()) < target && total > 0) {
+      chunk = round_up(std::max<int64_t>(kMinSplitTokens, ceil_div(total, target)), kKeyStep);
+      chunk = std::max<int64_t>(chunk, round_up(ceil_div(longest, UA_MAX_SPLITS), kKeyStep));
+      if (chunk >= longest) chunk = 0;
+    }
+  }
+  s.split_tokens = static_cast<int32_t>(chunk);
+  int64_t slot = 0;
+  for (const ua_tile& t : dec) {
+    const int64_t len = t.kv_hi - t.kv_lo;
+    int64_t pieces = 1, size = len;
+    if (p.num_splits > 0) {
+      pieces = std::max<int64_t>(1, std::min<int64_t>(p.num_splits, ceil_div(len, kKeyStep)));
+      size = round_up(ceil_div(len, pieces), kKeyStep);
+      pieces = std::max<int64_t>(1, ceil_div(len, size));
+    } else if (chunk > 0 && len > chunk) {
+      size = chunk;
+      pieces = ceil_div(len, chunk);
+    }
+    if (pieces <= 1) {
+      s.decode.push_back(t);
+      continue;
+    }
+    ua_combine_group grp;
+    grp.seq = t.seq;
+    grp.kv_head = t.kv_head;
+    grp.row0 = t.row0;
+    grp.nrows = t.nrows;
+    grp.slot0 = static_cast<int32_t>(slot);
+    grp.nsplits = static_cast<int32_t>(pieces);
+    grp.pad0 = grp.pad1 = 0;
+    const int32_t gid = static_cast<int32_t>(s.groups.size());
+    s.groups.push_back(grp);
+    for (int64_t k = 0; k < pieces; ++k) {
+      ua_tile piece = t;
+      piece.kv_lo = static_cast<int32_t>(t.kv_lo + k * size);
+      piece.kv_hi = static_cast<int32_t>(std::min<int64_t>(t.kv_hi, t.kv_lo + (k + 1) * size));
+      piece.slot = static_cast<int32_t>(slot++);
+      piece.group = gid;
+      s.decode.push_back(piece);
+    }
+  }
+  s.num_slots = slot;
+
+  // 3. Longest work first, so the tail of the grid holds the short tiles.
+  auto longer = [](const ua_tile& a, const ua_tile& b) {
+    const int64_t wa = static_cast<int64_t>(a.kv_hi - a.kv_lo) * a.nrows;
+    const int64_t wb = static_cast<int64_t>(b.kv_hi - b.kv_lo) * b.nrows;
+    if (wa != wb) return wa > wb;
+    if (a.seq != b.seq) return a.seq < b.seq;
+    if (a.kv_head != b.kv_head) return a.kv_head < b.kv_head;
+    if (a.row0 != b.row0) return a.row0 < b.row0;
+    return a.kv_lo < b.kv_lo;
+  };
+  std::stable_sort(s.decode.begin(), s.decode.end(), longer);
+  std::stable_sort(s.prefill.begin(), s.prefill.end(), longer);
+  *out = std::move(s);
+  return UA_OK;
+}
+
+int64_t workspace_bytes(const Schedule& s, int head_dim) {
+  return s.num_slots * UA_DECODE_ROWS * (static_cast<int64_t>(head_dim) + 1) *
+         static_cast<int64_t>(sizeof(float));
+}
+
+}  // namespace ua

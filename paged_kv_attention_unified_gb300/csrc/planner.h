@@ -1,0 +1,68 @@
+// Host-side work scheduler for the unified paged-KV attention forward.
+//
+// Replaces the per-program binary search over the query prefix sums and the
+// "2D or 3D kernel" choice of the vLLM Triton kernel
+// ("vllm_triton_unified_attention_notes", find_seq_idx and the unified_attention
+// host wrapper) with a precomputed, flat tile list built once per batch on the
+// CPU from host copies of the lengths.
+#pragma once
+
+#include <cstdint>
+#include <climits>
+#include <vector>
+
+#include "../../include/ua.h"
+
+namespace ua {
+
+struct Problem {
+  const int32_t* cu_query_lens = nullptr;  // host [num_seqs + 1]
+  const int32_t* kv_lens = nullptr;        // host [num_seqs]
+  int32_t num_seqs = 0;
+  int32_t num_q_heads = 0;
+  int32_t num_kv_heads = 0;
+  int32_t head_dim = 0;
+  int32_t block_size = 0;
+  int32_t max_blocks_per_seq = 0;
+  int32_t kv_dtype = UA_KV_BF16;
+  int32_t causal = 1;
+  int32_t window = 0;
+  int32_t num_splits = 0;       // 0: automatic
+  int32_t num_sms = 152;
+  int32_t decode_rows_max = -1; // < 0: default
+};
+
+struct Schedule {
+  std::vector<ua_tile> prefill;
+  std::vector<ua_tile> decode;
+  std::vector<ua_combine_group> groups;
+  int64_t num_slots = 0;
+  int32_t split_tokens = 0;
+  int32_t max_q = 0;
+  int32_t max_kv = 0;
+};
+
+// Granularity of key ranges: one decode step reads 16 tokens, so split pieces
+// and decode ranges start on multiples of 16.
+constexpr int kKeyStep = 16;
+// Decode kernel: resident CTAs per SM assumed when sizing automatic splits.
+constexpr int kDecodeCtasPerSm = 4;
+// Automatic splits aim for this many waves of decode CTAs.
+constexpr int kDecodeWaves = 2;
+// Smallest automatic split piece, in key tokens.
+constexpr int kMinSplitTokens = 256;
+// Default: sequences with q_len * qpk above this go to the prefill kernel
+// (every sequence goes to the decode kernel while no prefill kernel is built).
+constexpr int kDefaultDecodeRowsMax = INT32_MAX;
+
+// Validate the problem (host arrays included).
+ua_status validate(const Problem& p);
+
+// Validate and build the schedule.
+ua_status build_schedule(const Problem& p, Schedule* out);
+
+// Workspace bytes for a schedule: per slot, UA_DECODE_ROWS rows of head_dim
+// fp32 partial outputs plus UA_DECODE_ROWS fp32 log-sum-exp values.
+int64_t workspace_bytes(const Schedule& s, int head_dim);
+
+}  // namespace ua

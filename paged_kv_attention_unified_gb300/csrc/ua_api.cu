@@ -1,0 +1,443 @@
+// C ABI of the unified paged-KV attention forward (declared in include/ua.h):
+// plan creation around the CPU scheduler, argument validation, and the kernel
+// launches of one forward call.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "planner.h"
+#include "ua_kernels.h"
+
+struct ua_plan {
+  int device = 0;
+  ua::Problem prob;
+  ua::Schedule sched;
+  ua_plan_info info{};
+  // device memory owned by the plan
+  void* d_meta = nullptr;          // [prefill tiles | decode tiles | groups | error word]
+  ua_tile* d_prefill = nullptr;
+  ua_tile* d_decode = nullptr;
+  ua_combine_group* d_groups = nullptr;
+  int32_t* d_err = nullptr;
+  float* d_ws = nullptr;           // split workspace: partial rows then lse values
+  float* d_ws_o = nullptr;
+  float* d_ws_lse = nullptr;
+  cudaStream_t last_stream = nullptr;
+  // kernel timing (ua_plan_set_profiling)
+  struct EventPair {
+    cudaEvent_t start = nullptr, stop = nullptr;
+    int kind = 0;
+  };
+  bool profiling = false;
+  std::vector<EventPair> ev_pending, ev_free;
+};
+
+namespace {
+
+ua_status from_cuda(cudaError_t e) { return e == cudaSuccess ? UA_OK : UA_ERR_CUDA; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void free_plan_memory(ua_plan* p) {
+  for (auto* v : {&p->ev_pending, &p->ev_free})
+    for (auto& e : *v) {
+      if (e.start) cudaEventDestroy(e.start);
+      if (e.stop) cudaEventDestroy(e.stop);
+    }
+  p->ev_pending.clear();
+  p->ev_free.clear();
+  if (p->d_meta) cudaFree(p->d_meta);
+  if (p->d_ws) cudaFree(p->d_ws);
+  p->d_meta = nullptr;
+  p->d_ws = nullptr;
+}
+
+ua::Problem make_problem(const int32_t* cu, const int32_t* kv, int32_t num_seqs, int32_t hq,
+                         int32_t hkv, int32_t d, int32_t bs, int32_t max_blocks, int32_t dtype,
+                         int32_t causal, int32_t window, int32_t num_splits, int32_t num_sms,
+                         int32_t decode_rows_max) {
+  ua::Problem p;
+  p.cu_query_lens = cu;
+  p.kv_lens = kv;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = hq;
+  p.num_kv_heads = hkv;
+  p.head_dim = d;
+  p.block_size = bs;
+  p.max_blocks_per_seq = max_blocks;
+  p.kv_dtype = dtype;
+  p.causal = causal;
+  p.window = window;
+  p.num_splits = num_splits;
+  p.num_sms = num_sms;
+  p.decode_rows_max = decode_rows_max;
+  return p;
+}
+
+void fill_info(const ua::Schedule& s, int head_dim, int num_sms, ua_plan_info* info) {
+  info->num_prefill_tiles = static_cast<int64_t>(s.prefill.size());
+  info->num_decode_tiles = static_cast<int64_t>(s.decode.size());
+  info->num_combine_groups = static_cast<int64_t>(s.groups.size());
+  info->num_slots = s.num_slots;
+  info->workspace_bytes = ua::workspace_bytes(s, head_dim);
+  info->split_tokens = s.split_tokens;
+  info->num_sms = num_sms;
+}
+
+ua::KernelParams base_params(const ua_plan* plan, const void* q, const void* k, const void* v,
+                             void* out, const int32_t* cu, const int32_t* kvl, const int32_t* bt,
+                             int64_t num_blocks, float scale, float k_scale, float v_scale) {
+  const ua::Problem& pr = plan->prob;
+  ua::KernelParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.q = q;
+  kp.k_cache = k;
+  kp.v_cache = v;
+  kp.out = out;
+  kp.cu_query_lens = cu;
+  kp.kv_lens = kvl;
+  kp.block_tables = bt;
+  kp.ws_o = plan->d_ws_o;
+  kp.ws_lse = plan->d_ws_lse;
+  kp.err = plan->d_err;
+  kp.num_blocks = num_blocks;
+  kp.max_blocks_per_seq = pr.max_blocks_per_seq;
+  kp.block_size = pr.block_size;
+  kp.num_q_heads = pr.num_q_heads;
+  kp.num_kv_heads = pr.num_kv_heads;
+  kp.qpk = pr.num_q_heads / pr.num_kv_heads;
+  kp.causal = pr.causal;
+  kp.window = pr.window;
+  const bool fp8 = pr.kv_dtype == UA_KV_FP8_E4M3;
+  kp.score_scale_log2 = scale * ua::kLog2e * (fp8 ? k_scale : 1.f);
+  kp.v_scale = fp8 ? v_scale : 1.f;
+  return kp;
+}
+
+// Record the start event of a timed launch (no-op unless profiling).
+ua_plan::EventPair* timing_begin(ua_plan* p, int kind, cudaStream_t cs) {
+  if (!p->profiling) return nullptr;
+  ua_plan::EventPair e;
+  if (!p->ev_free.empty()) {
+    e = p->ev_free.back();
+    p->ev_free.pop_back();
+  } else if (cudaEventCreate(&e.start) != cudaSuccess || cudaEventCreate(&e.stop) != cudaSuccess) {
+    return nullptr;
+  }
+  e.kind = kind;
+  cudaEventRecord(e.start, cs);
+  p->ev_pending.push_back(e);
+  return &p->ev_pending.back();
+}
+
+void timing_end(ua_plan::EventPair* e, cudaStream_t cs) {
+  if (e) cudaEventRecord(e->stop, cs);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ua_status_string(int32_t status) {
+  switch (status) {
+    case UA_OK: return "UA_OK";
+    case UA_ERR_INVALID_ARG: return "UA_ERR_INVALID_ARG: invalid argument";
+    case UA_ERR_UNSUPPORTED: return "UA_ERR_UNSUPPORTED: head_dim, dtype or block_size not built";
+    case UA_ERR_CUDA: return "UA_ERR_CUDA: a CUDA call failed";
+    case UA_ERR_WORKSPACE: return "UA_ERR_WORKSPACE: workspace missing or too small";
+    case UA_ERR_DEVICE_TIMEOUT: return "UA_ERR_DEVICE_TIMEOUT: a device-side wait gave up";
+    case UA_ERR_BOUNDS: return "UA_ERR_BOUNDS: page id outside [0, num_blocks)";
+    default: return "unknown ua_status";
+  }
+}
+
+ua_status ua_schedule(const int32_t* cu_query_lens_host, const int32_t* kv_lens_host,
+                      int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                      int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                      int32_t kv_dtype, int32_t causal, int32_t window, int32_t num_splits,
+                      int32_t num_sms, int32_t decode_rows_max, ua_plan_info* info,
+                      ua_tile* prefill_tiles, int64_t prefill_cap, ua_tile* decode_tiles,
+                      int64_t decode_cap, ua_combine_group* groups, int64_t groups_cap) {
+  if (info == nullptr) return UA_ERR_INVALID_ARG;
+  const int sms = num_sms > 0 ? num_sms : 152;
+  ua::Problem pr = make_problem(cu_query_lens_host, kv_lens_host, num_seqs, num_q_heads,
+                                num_kv_heads, head_dim, block_size, max_blocks_per_seq, kv_dtype,
+                                causal, window, num_splits, sms, decode_rows_max);
+  ua::Schedule s;
+  try {
+    ua_status st = ua::build_schedule(pr, &s);
+    if (st != UA_OK) return st;
+  } catch (const std::bad_alloc&) {
+    return UA_ERR_INVALID_ARG;
+  }
+  fill_info(s, head_dim, sms, info);
+  if (prefill_tiles) {
+    if (prefill_cap < static_cast<int64_t>(s.prefill.size())) return UA_ERR_INVALID_ARG;
+    std::memcpy(prefill_tiles, s.prefill.data(), s.prefill.size() * sizeof(ua_tile));
+  }
+  if (decode_tiles) {
+    if (decode_cap < static_cast<int64_t>(s.decode.size())) return UA_ERR_INVALID_ARG;
+    std::memcpy(decode_tiles, s.decode.data(), s.decode.size() * sizeof(ua_tile));
+  }
+  if (groups) {
+    if (groups_cap < static_cast<int64_t>(s.groups.size())) return UA_ERR_INVALID_ARG;
+    std::memcpy(groups, s.groups.data(), s.groups.size() * sizeof(ua_combine_group));
+  }
+  return UA_OK;
+}
+
+ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
+                            const int32_t* kv_lens_host, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t max_blocks_per_seq, int32_t kv_dtype, int32_t causal,
+                            int32_t window, int32_t num_splits, int32_t decode_rows_max,
+                            ua_stream_t stream) {
+  if (out == nullptr) return UA_ERR_INVALID_ARG;
+  *out = nullptr;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return UA_ERR_CUDA;
+  ua_plan* plan = new (std::nothrow) ua_plan();
+  if (plan == nullptr) return UA_ERR_INVALID_ARG;
+  plan->device = dev;
+  plan->prob = make_problem(cu_query_lens_host, kv_lens_host, num_seqs, num_q_heads,
+                            num_kv_heads, head_dim, block_size, max_blocks_per_seq, kv_dtype,
+                            causal, window, num_splits, sms, decode_rows_max);
+  ua_status st;
+  try {
+    st = ua::build_schedule(plan->prob, &plan->sched);
+  } catch (const std::bad_alloc&) {
+    st = UA_ERR_INVALID_ARG;
+  }
+  if (st != UA_OK) {
+    delete plan;
+    return st;
+  }
+  // The plan keeps no pointer to the caller's host arrays.
+  plan->prob.cu_query_lens = nullptr;
+  plan->prob.kv_lens = nullptr;
+  fill_info(plan->sched, head_dim, sms, &plan->info);
+
+  const ua::Schedule& s = plan->sched;
+  const size_t n_pre = s.prefill.size(), n_dec = s.decode.size(), n_grp = s.groups.size();
+  const size_t bytes_tiles = (n_pre + n_dec) * sizeof(ua_tile);
+  const size_t bytes_groups = n_grp * sizeof(ua_combine_group);
+  const size_t bytes_meta = bytes_tiles + bytes_groups + 16;
+  std::vector<uint8_t> host(bytes_meta, 0);
+  if (n_pre) std::memcpy(host.data(), s.prefill.data(), n_pre * sizeof(ua_tile));
+  if (n_dec) std::memcpy(host.data() + n_pre * sizeof(ua_tile), s.decode.data(),
+                         n_dec * sizeof(ua_tile));
+  if (n_grp) std::memcpy(host.data() + bytes_tiles, s.groups.data(), bytes_groups);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMalloc(&plan->d_meta, bytes_meta) != cudaSuccess) {
+    free_plan_memory(plan);
+    delete plan;
+    return UA_ERR_CUDA;
+  }
+  uint8_t* base = static_cast<uint8_t*>(plan->d_meta);
+  plan->d_prefill = reinterpret_cast<ua_tile*>(base);
+  plan->d_decode = reinterpret_cast<ua_tile*>(base + n_pre * sizeof(ua_tile));
+  plan->d_groups = reinterpret_cast<ua_combine_group*>(base + bytes_tiles);
+  plan->d_err = reinterpret_cast<int32_t*>(base + bytes_tiles + bytes_groups);
+  if (plan->info.workspace_bytes > 0) {
+    if (cudaMalloc(&plan->d_ws, static_cast<size_t>(plan->info.workspace_bytes)) != cudaSuccess) {
+      free_plan_memory(plan);
+      delete plan;
+      return UA_ERR_CUDA;
+    }
+    plan->d_ws_o = static_cast<float*>(plan->d_ws);
+    plan->d_ws_lse = plan->d_ws_o + s.num_slots * UA_DECODE_ROWS * static_cast<int64_t>(head_dim);
+  }
+  if (cudaMemcpyAsync(plan->d_meta, host.data(), bytes_meta, cudaMemcpyHostToDevice, cs) !=
+      cudaSuccess) {
+    free_plan_memory(plan);
+    delete plan;
+    return UA_ERR_CUDA;
+  }
+  plan->last_stream = cs;
+  *out = plan;
+  return UA_OK;
+}
+
+ua_status ua_plan_create(ua_plan** out, const int32_t* cu_query_lens_host,
+                         const int32_t* kv_lens_host, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t max_blocks_per_seq, int32_t kv_dtype, int32_t causal,
+                         int32_t window, int32_t num_splits, ua_stream_t stream) {
+  return ua_plan_create_ex(out, cu_query_lens_host, kv_lens_host, num_seqs, num_q_heads,
+                           num_kv_heads, head_dim, block_size, max_blocks_per_seq, kv_dtype,
+                           causal, window, num_splits, -1, stream);
+}
+
+ua_status ua_plan_get_info(const ua_plan* plan, ua_plan_info* info) {
+  if (plan == nullptr || info == nullptr) return UA_ERR_INVALID_ARG;
+  *info = plan->info;
+  return UA_OK;
+}
+
+ua_status ua_plan_destroy(ua_plan* plan) {
+  if (plan == nullptr) return UA_OK;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  if (cur != plan->device) cudaSetDevice(plan->device);
+  cudaStreamSynchronize(plan->last_stream);
+  free_plan_memory(plan);
+  if (cur != plan->device) cudaSetDevice(cur);
+  delete plan;
+  return UA_OK;
+}
+
+ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
+                     const void* v_cache, void* out, const int32_t* cu_query_lens,
+                     const int32_t* kv_lens, const int32_t* block_tables, int64_t num_blocks,
+                     int32_t max_q, int32_t max_kv, float scale, float k_scale, float v_scale,
+                     ua_stream_t stream) {
+  if (plan == nullptr) return UA_ERR_INVALID_ARG;
+  const ua::Schedule& s = plan->sched;
+  const bool any = !s.prefill.empty() || !s.decode.empty();
+  if (!any) return UA_OK;
+  if (!q || !k_cache || !v_cache || !out || !cu_query_lens || !kv_lens || !block_tables)
+    return UA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return UA_ERR_INVALID_ARG;
+  if (num_blocks <= 0 || max_q < s.max_q || max_kv < s.max_kv) return UA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return UA_ERR_INVALID_ARG;
+  if (plan->prob.kv_dtype == UA_KV_FP8_E4M3 && (!std::isfinite(k_scale) || !std::isfinite(v_scale)))
+    return UA_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UA_ERR_CUDA;
+  if (dev != plan->device) return UA_ERR_INVALID_ARG;
+  if (!s.prefill.empty()) return UA_ERR_UNSUPPORTED;  // prefill kernel not linked in this build
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  ua_plan* mp = const_cast<ua_plan*>(plan);
+  mp->last_stream = cs;
+  ua::KernelParams kp = base_params(plan, q, k_cache, v_cache, out, cu_query_lens, kv_lens,
+                                    block_tables, num_blocks, scale, k_scale, v_scale);
+  if (!s.decode.empty()) {
+    kp.tiles = plan->d_decode;
+    kp.num_tiles = static_cast<int32_t>(s.decode.size());
+    auto* ev = timing_begin(mp, 1, cs);
+    if (ua::launch_decode(kp, plan->prob.head_dim, plan->prob.kv_dtype, cs) != cudaSuccess)
+      return UA_ERR_CUDA;
+    timing_end(ev, cs);
+  }
+  if (!s.groups.empty()) {
+    ua::CombineParams cp;
+    cp.groups = plan->d_groups;
+    cp.num_groups = static_cast<int32_t>(s.groups.size());
+    cp.ws_o = plan->d_ws_o;
+    cp.ws_lse = plan->d_ws_lse;
+    cp.cu_query_lens = cu_query_lens;
+    cp.out = out;
+    cp.num_q_heads = plan->prob.num_q_heads;
+    cp.qpk = plan->prob.num_q_heads / plan->prob.num_kv_heads;
+    auto* ev = timing_begin(mp, 2, cs);
+    if (ua::launch_combine(cp, plan->prob.head_dim, cs) != cudaSuccess) return UA_ERR_CUDA;
+    timing_end(ev, cs);
+  }
+  return UA_OK;
+}
+
+ua_status ua_forward_oneshot(const void* q, const void* k_cache, const void* v_cache, void* out,
+                             const int32_t* cu_query_lens_host, const int32_t* kv_lens_host,
+                             const int32_t* cu_query_lens, const int32_t* kv_lens,
+                             const int32_t* block_tables, int32_t num_seqs,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t block_size, int32_t max_blocks_per_seq,
+                             int64_t num_blocks, int32_t kv_dtype, int32_t max_q,
+                             int32_t max_kv, float scale, int32_t causal, int32_t window,
+                             float k_scale, float v_scale, int32_t num_splits,
+                             ua_stream_t stream) {
+  ua_plan* plan = nullptr;
+  ua_status st = ua_plan_create(&plan, cu_query_lens_host, kv_lens_host, num_seqs, num_q_heads,
+                                num_kv_heads, head_dim, block_size, max_blocks_per_seq, kv_dtype,
+                                causal, window, num_splits, stream);
+  if (st != UA_OK) return st;
+  st = ua_forward(plan, q, k_cache, v_cache, out, cu_query_lens, kv_lens, block_tables,
+                  num_blocks, max_q, max_kv, scale, k_scale, v_scale, stream);
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess &&
+      st == UA_OK)
+    st = UA_ERR_CUDA;
+  ua_plan_destroy(plan);
+  return st;
+}
+
+ua_status ua_last_device_error(ua_plan* plan, int32_t* code) {
+  if (plan == nullptr || code == nullptr) return UA_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(plan->last_stream) != cudaSuccess) return UA_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, plan->d_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return UA_ERR_CUDA;
+  const int32_t zero = 0;
+  if (cudaMemcpy(plan->d_err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return UA_ERR_CUDA;
+  *code = v;
+  return UA_OK;
+}
+
+ua_status ua_gather_kv_debug(const ua_plan* plan, const void* k_cache, const void* v_cache,
+                             const int32_t* kv_lens, const int32_t* block_tables,
+                             int64_t num_blocks, void* k_out, void* v_out, int64_t rows_cap,
+                             ua_stream_t stream) {
+  if (plan == nullptr || !k_cache || !v_cache || !kv_lens || !block_tables || !k_out || !v_out)
+    return UA_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_out) || !aligned16(v_out) ||
+      num_blocks <= 0)
+    return UA_ERR_INVALID_ARG;
+  const ua::Schedule& s = plan->sched;
+  // Row offsets from the host ranges; the kernel clamps by the device kv_lens,
+  // which the caller guarantees equal the plan's.
+  std::vector<int64_t> offs(s.decode.size() + 1, 0);
+  for (size_t i = 0; i < s.decode.size(); ++i)
+    offs[i + 1] = offs[i] + (s.decode[i].kv_hi - s.decode[i].kv_lo);
+  if (offs.back() > rows_cap) return UA_ERR_INVALID_ARG;
+  if (s.decode.empty()) return UA_OK;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int64_t* d_offs = nullptr;
+  if (cudaMalloc(&d_offs, offs.size() * sizeof(int64_t)) != cudaSuccess) return UA_ERR_CUDA;
+  ua_status st = from_cuda(cudaMemcpyAsync(d_offs, offs.data(), offs.size() * sizeof(int64_t),
+                                           cudaMemcpyHostToDevice, cs));
+  if (st == UA_OK) {
+    ua::KernelParams kp = base_params(plan, nullptr, k_cache, v_cache, nullptr, nullptr, kv_lens,
+                                      block_tables, num_blocks, 1.f, 1.f, 1.f);
+    kp.tiles = plan->d_decode;
+    kp.num_tiles = static_cast<int32_t>(s.decode.size());
+    const int elt = plan->prob.kv_dtype == UA_KV_FP8_E4M3 ? 1 : 2;
+    st = from_cuda(ua::launch_gather_debug(kp, d_offs, plan->prob.head_dim, elt, k_out, v_out, cs));
+  }
+  if (cudaStreamSynchronize(cs) != cudaSuccess && st == UA_OK) st = UA_ERR_CUDA;
+  cudaFree(d_offs);
+  return st;
+}
+
+ua_status ua_plan_set_profiling(ua_plan* plan, int32_t enable) {
+  if (plan == nullptr) return UA_ERR_INVALID_ARG;
+  plan->profiling = enable != 0;
+  return UA_OK;
+}
+
+ua_status ua_plan_kernel_times(ua_plan* plan, float* ms, int64_t* launches) {
+  if (plan == nullptr || ms == nullptr || launches == nullptr) return UA_ERR_INVALID_ARG;
+  for (int k = 0; k < 3; ++k) {
+    ms[k] = 0.f;
+    launches[k] = 0;
+  }
+  if (cudaStreamSynchronize(plan->last_stream) != cudaSuccess) return UA_ERR_CUDA;
+  ua_status st = UA_OK;
+  for (auto& e : plan->ev_pending) {
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, e.start, e.stop) != cudaSuccess) st = UA_ERR_CUDA;
+    ms[e.kind] += t;
+    launches[e.kind] += 1;
+    plan->ev_free.push_back(e);
+  }
+  plan->ev_pending.clear();
+  return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,207 @@
+"""C-ABI library checks that need no GPU: exports, validation, the scheduler.
+
+The scheduler's tile lists are compared with a brute-force enumeration of
+which rows exist and which keys each row can see (exact integer equality).
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_attention_unified_gb300 as ua
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from paged_kv_attention_unified_gb300 import build
+    build.build()
+
+
+def _header_functions():
+    txt = open(os.path.join(ROOT, "include", "ua.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^(?:ua_status|const char\*)\s+(ua_\w+)\s*\(", txt, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    names = _header_functions()
+    assert len(names) >= 10
+    assert sorted(ua.EXPORTS) == names
+    lib = ua.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    for code in range(-6, 1):
+        s = ua.ua_status_string(code)
+        assert s and "unknown" not in s
+    assert "unknown" in ua.ua_status_string(-99)
+
+
+BAD = [
+    dict(cu=[0, 1], kv=[0]),                         # kv_len < q_len
+    dict(cu=[1, 2], kv=[5]),                         # cu[0] != 0
+    dict(cu=[0, 3, 2], kv=[5, 5]),                   # negative q_len
+    dict(cu=[0, 1], kv=[5], hq=6, hkv=4),            # Hq % Hkv != 0
+    dict(cu=[0, 1], kv=[500], max_blocks=2),          # page table too short
+    dict(cu=[0, 1], kv=[5], num_splits=129),          # too many splits
+    dict(cu=[0, 1], kv=[5], dtype=7),                 # unknown dtype
+    dict(cu=[0, 1], kv=[-1]),                         # negative kv_len
+]
+
+
+@pytest.mark.parametrize("bad", BAD)
+def test_invalid_problems_are_rejected(bad):
+    with pytest.raises(ua.UAError) as e:
+        ua.ua_schedule(bad["cu"], bad["kv"], bad.get("hq", 4), bad.get("hkv", 4), 128, 16,
+                       bad.get("max_blocks", 64), kv_dtype=bad.get("dtype", 0),
+                       num_splits=bad.get("num_splits", 0))
+    assert e.value.status == ua.UA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d,bs", [(96, 16), (128, 8), (256, 16), (64, 24)])
+def test_unsupported_shapes(d, bs):
+    with pytest.raises(ua.UAError) as e:
+        ua.ua_schedule([0, 1], [5], 4, 4, d, bs, 64)
+    assert e.value.status == ua.UA_ERR_UNSUPPORTED
+
+
+def test_empty_batch_schedules_nothing():
+    info, pre, dec, grp = ua.ua_schedule([0], [], 4, 4, 128, 16, 1)
+    assert (info.num_prefill_tiles, info.num_decode_tiles, info.num_combine_groups) == (0, 0, 0)
+    info, pre, dec, grp = ua.ua_schedule([0, 0, 0], [0, 7], 4, 4, 128, 16, 1)
+    assert info.num_decode_tiles == 0 and info.num_prefill_tiles == 0
+
+
+def _visible(kv, ql, i, causal, window):
+    """Every key position, tested one by one (vectorised with numpy)."""
+    pos = kv - ql + i
+    t = np.arange(kv)
+    keep = np.ones(kv, dtype=bool)
+    if causal:
+        keep &= ~(t > pos)
+    if window > 0:
+        keep &= ~(t <= pos - window)
+    return t[keep]
+
+
+def _check_schedule(cu, kv, hq, hkv, causal=1, window=0, num_splits=0, num_sms=152,
+                    decode_rows_max=-1):
+    info, pre, dec, grp = ua.ua_schedule(cu, kv, hq, hkv, 128, 16, 1 + max(kv) // 16 + 1,
+                                         causal=causal, window=window, num_splits=num_splits,
+                                         num_sms=num_sms, decode_rows_max=decode_rows_max)
+    qpk = hq // hkv
+    rows_max = (2 ** 31 - 1) if decode_rows_max < 0 else decode_rows_max
+    seen = {}
+    for kind, tiles, rows_per in (("pre", pre, 128), ("dec", dec, 8)):
+        for t in tiles:
+            assert 1 <= t["nrows"] <= rows_per
+            for r in range(t["row0"], t["row0"] + t["nrows"]):
+                key = (t["seq"], t["kv_head"], r)
+                seen.setdefault(key, []).append((kind, t))
+    # every (seq, kv head, row) exists exactly once (split pieces share a row)
+    expected = set()
+    for s in range(len(kv)):
+        ql = cu[s + 1] - cu[s]
+        for g in range(hkv):
+            for r in range(ql * qpk):
+                expected.add((s, g, r))
+    assert set(seen) == expected
+    bounds = {}
+    for (s, g, r), owners in seen.items():
+        ql = cu[s + 1] - cu[s]
+        kind = owners[0][0]
+        assert all(k == kind for k, _ in owners)
+        assert kind == ("dec" if ql * qpk <= rows_max else "pre")
+        pieces = sorted((t["kv_lo"], t["kv_hi"]) for _, t in owners)
+        # pieces are contiguous and disjoint
+        for (a0, a1), (b0, b1) in zip(pieces, pieces[1:]):
+            assert a1 == b0
+        lo, hi = pieces[0][0], pieces[-1][1]
+        # the tile's range is exactly the floor-16 of the lowest and one past the
+        # highest key visible to any of its rows
+        t0 = owners[0][1]
+        bkey = (s, t0["row0"], t0["nrows"])
+        if bkey not in bounds:
+            vmin, vmax = None, None
+            for i in sorted({rr // qpk for rr in range(t0["row0"], t0["row0"] + t0["nrows"])}):
+                v = _visible(kv[s], ql, i, causal, window)
+                vmin = v.min() if vmin is None else min(vmin, v.min())
+                vmax = v.max() if vmax is None else max(vmax, v.max())
+            bounds[bkey] = (vmin, vmax)
+        vmin, vmax = bounds[bkey]
+        assert hi == vmax + 1
+        assert lo == (vmin // 16) * 16
+        assert lo % 16 == 0 and all(p[0] % 16 == 0 for p in pieces)
+        assert hi <= kv[s]
+        if len(owners) > 1:
+            assert len(owners) <= 128
+            gids = {t["group"] for _, t in owners}
+            assert len(gids) == 1
+            gg = grp[gids.pop()]
+            assert gg["nsplits"] == len(owners)
+            assert sorted(t["slot"] for _, t in owners) == list(
+                range(gg["slot0"], gg["slot0"] + gg["nsplits"]))
+            if num_splits > 0:
+                assert len(owners) <= num_splits
+        else:
+            assert owners[0][1]["slot"] == -1 and owners[0][1]["group"] == -1
+    # slots are used once each
+    slots = [t["slot"] for t in dec if t["slot"] >= 0]
+    assert sorted(slots) == list(range(info.num_slots))
+    # longest-first order
+    work = [(t["kv_hi"] - t["kv_lo"]) * t["nrows"] for t in dec]
+    assert work == sorted(work, reverse=True)
+    return info, pre, dec, grp
+
+
+def test_schedule_tiny_mixed():
+    _check_schedule([0, 1, 6, 23], [40, 130, 300], 4, 4)
+
+
+def test_schedule_tiny_mixed_with_prefill_kernel():
+    _check_schedule([0, 1, 6, 23], [40, 130, 300], 4, 4, decode_rows_max=16)
+
+
+@pytest.mark.parametrize("ns", [1, 2, 3, 16, 128])
+def test_schedule_forced_splits(ns):
+    _check_schedule([0, 1, 2, 4], [3000, 17, 900], 32, 8, num_splits=ns)
+
+
+def test_schedule_window_and_noncausal():
+    _check_schedule([0, 3, 4, 40], [100, 1000, 70], 8, 2, window=37)
+    _check_schedule([0, 3, 4, 40], [100, 1000, 70], 8, 2, causal=0)
+    _check_schedule([0, 3, 4, 40], [100, 1000, 70], 8, 2, causal=0, window=5,
+                    decode_rows_max=8)
+
+
+def test_schedule_auto_splits_long_decode():
+    info, _, dec, grp = _check_schedule([0] + list(range(1, 9)), [131072] * 8, 64, 8)
+    assert all(g["nsplits"] >= 16 for g in grp)
+    assert info.num_combine_groups == 64
+    assert info.workspace_bytes == info.num_slots * 8 * 129 * 4
+
+
+def test_schedule_random_brute_force():
+    import random
+    rng = random.Random(0)
+    for it in range(30):
+        B = rng.randint(1, 6)
+        hkv = rng.choice([1, 2, 4])
+        hq = hkv * rng.choice([1, 2, 4, 8, 16])
+        cu, kv = [0], []
+        for _ in range(B):
+            k = rng.randint(0, 600)
+            q = rng.choice([0, 1, rng.randint(0, k), k]) if k else 0
+            q = min(q, k)
+            cu.append(cu[-1] + q)
+            kv.append(k)
+        if max(kv) == 0:
+            kv[0] = 1
+        _check_schedule(cu, kv, hq, hkv, causal=rng.choice([0, 1]), window=rng.choice([0, 0, 9]),
+                        num_splits=rng.choice([0, 0, 1, 3, 7]), num_sms=rng.choice([2, 152]),
+                        decode_rows_max=rng.choice([-1, 8, 32]))
