@@ -232,6 +232,46 @@ ua_status ua_gather_kv_debug(const ua_plan* plan, const void* k_cache, const voi
                              int64_t num_blocks, void* k_out, void* v_out, int64_t rows_cap,
                              ua_stream_t stream);
 
+/*
+ * ua_forward_static_scratch -- the same attention for callers that cannot
+ * allocate device memory. The pages describe no such entry point; it exists
+ * for code that runs inside another runtime owning every device allocation
+ * (its own memory pool, a plugin host), or in loops where cudaMalloc, which
+ * can synchronise the whole device, is not acceptable.
+ *
+ * It allocates nothing: the tile list, combine groups, split partials and
+ * error word live in one static device array of 16 MiB inside libua.so,
+ * which every GPU that loads the library keeps until the process exits. The
+ * tile list is built on the device from the device copies of the lengths
+ * (one tile per sequence, KV head, block of 8 packed rows and split), and every
+ * sequence runs through the split-KV decode kernel and the combine kernel.
+ *
+ * Arguments as ua_forward_oneshot, without host lengths: max_q / max_kv must
+ * bound every q_len / kv_len (max_q sizes the tile grid); num_splits 0 picks
+ * ceil(max_kv / 1024) pieces (at most UA_MAX_SPLITS, fewer if needed to fit),
+ * n > 0 uses exactly n. device_error: optional device int32 that receives the
+ * call's error word (UA_OK or UA_ERR_BOUNDS); may be NULL.
+ * Returns UA_ERR_WORKSPACE when the call's scratch (32 B per tile and per
+ * group, plus 8 * (head_dim + 1) * 4 B per tile when split) exceeds 16 MiB;
+ * nothing is launched then.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. Every call shares the one array and leaves its
+ * contents behind: calls whose work overlaps on the GPU (different streams,
+ * or different host threads) race on it and must be ordered by the caller.
+ */
+ua_status ua_forward_static_scratch(const void* q, const void* k_cache, const void* v_cache,
+                                    void* out, const int32_t* cu_query_lens,
+                                    const int32_t* kv_lens, const int32_t* block_tables,
+                                    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, int32_t block_size,
+                                    int32_t max_blocks_per_seq, int64_t num_blocks,
+                                    int32_t kv_dtype, int32_t max_q, int32_t max_kv, float scale,
+                                    int32_t causal, int32_t window, float k_scale, float v_scale,
+                                    int32_t num_splits, int32_t* device_error,
+                                    ua_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

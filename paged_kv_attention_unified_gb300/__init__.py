@@ -33,6 +33,7 @@ EXPORTS = (
     "ua_schedule", "ua_plan_create", "ua_plan_create_ex", "ua_forward", "ua_forward_oneshot",
     "ua_plan_get_info", "ua_last_device_error", "ua_plan_destroy", "ua_status_string",
     "ua_gather_kv_debug", "ua_plan_set_profiling", "ua_plan_kernel_times",
+    "ua_forward_static_scratch",
 )
 
 
@@ -86,6 +87,9 @@ _SIGS = {
     "ua_plan_destroy": (_I32, [_P]),
     "ua_gather_kv_debug": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _P, _I64, _P]),
     "ua_plan_set_profiling": (_I32, [_P, _I32]),
+    "ua_forward_static_scratch": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
+                                         _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32, _I32, _F,
+                                         _F, _I32, _P, _P]),
     "ua_plan_kernel_times": (_I32, [_P, ctypes.POINTER(ctypes.c_float),
                                     ctypes.POINTER(ctypes.c_int64)]),
 }
@@ -231,6 +235,24 @@ def ua_plan_kernel_times(plan: int):
     n = (ctypes.c_int64 * 3)()
     _check(lib().ua_plan_kernel_times(plan, ms, n), "ua_plan_kernel_times")
     return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def ua_forward_static_scratch(q, k_cache, v_cache, out, cu_query_lens, kv_lens, block_tables,
+                              num_q_heads, num_kv_heads, head_dim, block_size,
+                              max_blocks_per_seq, num_blocks, kv_dtype, max_q, max_kv, scale,
+                              causal=1, window=0, k_scale=1.0, v_scale=1.0, num_splits=0,
+                              device_error=None, stream=None):
+    """The forward without any device allocation (scratch in a static device
+    array inside libua.so); for callers that may not allocate device memory."""
+    ptr = lambda t: t if isinstance(t, int) else t.data_ptr()
+    n = int(kv_lens.numel()) if hasattr(kv_lens, "numel") else int(len(kv_lens))
+    _check(lib().ua_forward_static_scratch(
+        ptr(q), ptr(k_cache), ptr(v_cache), ptr(out), ptr(cu_query_lens), ptr(kv_lens),
+        ptr(block_tables), n, num_q_heads, num_kv_heads, head_dim, block_size,
+        max_blocks_per_seq, int(num_blocks), kv_dtype, int(max_q), int(max_kv), float(scale),
+        causal, window, float(k_scale), float(v_scale), num_splits,
+        None if device_error is None else ptr(device_error), _stream_handle(stream)),
+        "ua_forward_static_scratch")
 
 
 class Plan:
