@@ -209,6 +209,14 @@ ua_status ua_plan_get_info(const ua_plan* plan, ua_plan_info* info);
 ua_status ua_plan_set_profiling(ua_plan* plan, int32_t enable);
 ua_status ua_plan_kernel_times(ua_plan* plan, float* ms, int64_t* launches);
 
+/* Test aid for the device-side failure path. flags bit 0 makes the prefill
+ * kernel's TMA producer issue nothing, so its consumers' bounded waits run
+ * out: the kernel records UA_ERR_DEVICE_TIMEOUT in the error word, drains
+ * and frees what it holds, and exits (the output of the affected tiles is
+ * undefined). wait_timeout_ns bounds every device-side wait (0: 2 s default).
+ * Both apply to later ua_forward calls on this plan. */
+ua_status ua_plan_set_debug(ua_plan* plan, int32_t flags, int64_t wait_timeout_ns);
+
 /* Synchronises the plan's last stream, reads the device error word
  * (UA_OK, UA_ERR_BOUNDS or UA_ERR_DEVICE_TIMEOUT) into *code and clears it. */
 ua_status ua_last_device_error(ua_plan* plan, int32_t* code);

@@ -33,7 +33,7 @@ EXPORTS = (
     "ua_schedule", "ua_plan_create", "ua_plan_create_ex", "ua_forward", "ua_forward_oneshot",
     "ua_plan_get_info", "ua_last_device_error", "ua_plan_destroy", "ua_status_string",
     "ua_gather_kv_debug", "ua_plan_set_profiling", "ua_plan_kernel_times",
-    "ua_forward_static_scratch",
+    "ua_forward_static_scratch", "ua_plan_set_debug",
 )
 
 
@@ -87,6 +87,7 @@ _SIGS = {
     "ua_plan_destroy": (_I32, [_P]),
     "ua_gather_kv_debug": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _P, _I64, _P]),
     "ua_plan_set_profiling": (_I32, [_P, _I32]),
+    "ua_plan_set_debug": (_I32, [_P, _I32, _I64]),
     "ua_forward_static_scratch": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
                                          _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32, _I32, _F,
                                          _F, _I32, _P, _P]),
@@ -224,6 +225,11 @@ def ua_gather_kv_debug(plan, k_cache, v_cache, kv_lens, block_tables, num_blocks
 
 def ua_plan_set_profiling(plan: int, enable: bool):
     _check(lib().ua_plan_set_profiling(plan, 1 if enable else 0), "ua_plan_set_profiling")
+
+
+def ua_plan_set_debug(plan: int, flags: int, wait_timeout_ns: int = 0):
+    """Test aid: flags bit 0 idles the prefill producer (bounded waits run out)."""
+    _check(lib().ua_plan_set_debug(plan, int(flags), int(wait_timeout_ns)), "ua_plan_set_debug")
 
 
 KERNEL_KINDS = ("prefill", "decode", "combine")

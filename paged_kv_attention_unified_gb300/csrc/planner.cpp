@@ -66,7 +66,8 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
   if (st != UA_OK) return st;
   Schedule s;
   const int qpk = p.num_q_heads / p.num_kv_heads;
-  const int64_t rows_max = p.decode_rows_max < 0 ? kDefaultDecodeRowsMax : p.decode_rows_max;
+  const int64_t rows_max = !p.prefill_ok ? INT64_MAX
+                           : (p.decode_rows_max < 0 ? kDefaultDecodeRowsMax : p.decode_rows_max);
   const int num_sms = p.num_sms > 0 ? p.num_sms : 152;
 
   // 1. Whole decode tiles (before splitting) and prefill tiles.
@@ -89,6 +90,7 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
         t.row0 = static_cast<int32_t>(r0);
         t.nrows = static_cast<int32_t>(std::min<int64_t>(step, rows - r0));
         key_range(p, ctx, kv, t.row0, t.nrows, &t.kv_lo, &t.kv_hi);
+        if (!is_decode) t.kv_lo = static_cast<int32_t>(round_down(t.kv_lo, kPrefillKeyTile));
         t.slot = -1;
         t.group = -1;
         (is_decode ? dec : s.prefill).push_back(t);

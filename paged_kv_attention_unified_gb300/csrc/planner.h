@@ -30,6 +30,7 @@ struct Problem {
   int32_t num_splits = 0;       // 0: automatic
   int32_t num_sms = 152;
   int32_t decode_rows_max = -1; // < 0: default
+  bool prefill_ok = false;      // the prefill kernel can take this problem
 };
 
 struct Schedule {
@@ -52,8 +53,10 @@ constexpr int kDecodeWaves = 2;
 // Smallest automatic split piece, in key tokens.
 constexpr int kMinSplitTokens = 256;
 // Default: sequences with q_len * qpk above this go to the prefill kernel
-// (every sequence goes to the decode kernel while no prefill kernel is built).
-constexpr int kDefaultDecodeRowsMax = INT32_MAX;
+// (when it can take the problem; otherwise every sequence is decode work).
+constexpr int kDefaultDecodeRowsMax = 32;
+// Key tile of the prefill kernel: its key ranges start on multiples of this.
+constexpr int kPrefillKeyTile = 128;
 
 // Validate the problem (host arrays included).
 ua_status validate(const Problem& p);

@@ -3,6 +3,7 @@
 // launches of one forward call.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <new>
@@ -26,6 +27,9 @@ struct ua_plan {
   float* d_ws_o = nullptr;
   float* d_ws_lse = nullptr;
   cudaStream_t last_stream = nullptr;
+  int64_t total_q = 0;             // query tokens of the batch (host lengths)
+  int32_t debug_flags = 0;         // ua_plan_set_debug
+  uint64_t wait_timeout_ns = 2000000000ull;
   // kernel timing (ua_plan_set_profiling)
   struct EventPair {
     cudaEvent_t start = nullptr, stop = nullptr;
@@ -74,6 +78,7 @@ ua::Problem make_problem(const int32_t* cu, const int32_t* kv, int32_t num_seqs,
   p.num_splits = num_splits;
   p.num_sms = num_sms;
   p.decode_rows_max = decode_rows_max;
+  p.prefill_ok = hkv > 0 && hq % hkv == 0 && ua::prefill_supported(d, dtype, hq / hkv, bs);
   return p;
 }
 
@@ -217,6 +222,7 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
     delete plan;
     return st;
   }
+  plan->total_q = num_seqs > 0 ? cu_query_lens_host[num_seqs] : 0;
   // The plan keeps no pointer to the caller's host arrays.
   plan->prob.cu_query_lens = nullptr;
   plan->prob.kv_lens = nullptr;
@@ -311,13 +317,40 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return UA_ERR_CUDA;
   if (dev != plan->device) return UA_ERR_INVALID_ARG;
-  if (!s.prefill.empty()) return UA_ERR_UNSUPPORTED;  // prefill kernel not linked in this build
+  if (!s.prefill.empty() && num_blocks >= INT32_MAX) return UA_ERR_INVALID_ARG;  // TMA coordinate
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   ua_plan* mp = const_cast<ua_plan*>(plan);
   mp->last_stream = cs;
   ua::KernelParams kp = base_params(plan, q, k_cache, v_cache, out, cu_query_lens, kv_lens,
                                     block_tables, num_blocks, scale, k_scale, v_scale);
+  if (!s.prefill.empty()) {
+    ua::PrefillParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.tiles = plan->d_prefill;
+    pp.num_tiles = static_cast<int32_t>(s.prefill.size());
+    pp.cu_query_lens = cu_query_lens;
+    pp.kv_lens = kv_lens;
+    pp.block_tables = block_tables;
+    pp.out = out;
+    pp.err = plan->d_err;
+    pp.num_blocks = num_blocks;
+    pp.max_blocks_per_seq = plan->prob.max_blocks_per_seq;
+    pp.block_size = plan->prob.block_size;
+    pp.num_q_heads = plan->prob.num_q_heads;
+    pp.qpk = kp.qpk;
+    pp.causal = plan->prob.causal;
+    pp.window = plan->prob.window;
+    pp.score_scale_log2 = kp.score_scale_log2;
+    pp.rows_per_box = plan->prob.block_size < 128 ? plan->prob.block_size : 128;
+    pp.timeout_ns = plan->wait_timeout_ns;
+    pp.debug_flags = plan->debug_flags;
+    auto* ev = timing_begin(mp, 0, cs);
+    if (ua::launch_prefill(pp, q, k_cache, v_cache, plan->total_q, plan->prob.head_dim,
+                           plan->prob.num_kv_heads, cs) != cudaSuccess)
+      return UA_ERR_CUDA;
+    timing_end(ev, cs);
+  }
   if (!s.decode.empty()) {
     kp.tiles = plan->d_decode;
     kp.num_tiles = static_cast<int32_t>(s.decode.size());
@@ -438,6 +471,14 @@ ua_status ua_plan_kernel_times(ua_plan* plan, float* ms, int64_t* launches) {
   }
   plan->ev_pending.clear();
   return st;
+}
+
+ua_status ua_plan_set_debug(ua_plan* plan, int32_t flags, int64_t wait_timeout_ns) {
+  if (plan == nullptr || flags < 0 || wait_timeout_ns < 0) return UA_ERR_INVALID_ARG;
+  plan->debug_flags = flags;
+  plan->wait_timeout_ns = wait_timeout_ns > 0 ? static_cast<uint64_t>(wait_timeout_ns)
+                                              : 2000000000ull;
+  return UA_OK;
 }
 
 }  // extern "C"

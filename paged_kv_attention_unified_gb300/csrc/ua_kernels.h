@@ -7,6 +7,40 @@
 
 namespace ua {
 
+struct PrefillParams {
+  const ua_tile* tiles;
+  int32_t num_tiles;
+  const int32_t* cu_query_lens;
+  const int32_t* kv_lens;
+  const int32_t* block_tables;
+  void* out;
+  int32_t* err;
+  int64_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t block_size;
+  int32_t num_q_heads;
+  int32_t qpk;
+  int32_t causal;
+  int32_t window;
+  float score_scale_log2;   // scale * log2(e)
+  int32_t rows_per_box;     // keys per TMA box: min(block_size, 128)
+  uint64_t timeout_ns;      // bound of every mbarrier wait
+  int32_t debug_flags;      // bit 0: the producer issues nothing (timeout test)
+};
+
+// Bit 0 of PrefillParams::debug_flags: the TMA producer skips every load, so
+// that the consumers' bounded waits run out (tests the timeout path).
+constexpr int32_t kDebugProducerIdle = 1;
+
+// Whether the prefill kernel can take a problem with these parameters
+// (host-only check, no CUDA call).
+bool prefill_supported(int head_dim, int kv_dtype, int qpk, int block_size);
+
+// Prefill kernel over p.tiles (the host encodes the tensor maps from the pointers).
+cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_cache,
+                           const void* v_cache, int64_t total_q, int head_dim,
+                           int num_kv_heads, cudaStream_t stream);
+
 // Split-KV decode kernel over p.tiles[0 .. p.num_tiles).
 cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cudaStream_t stream);
 

@@ -95,7 +95,9 @@ def _check_schedule(cu, kv, hq, hkv, causal=1, window=0, num_splits=0, num_sms=1
                                          causal=causal, window=window, num_splits=num_splits,
                                          num_sms=num_sms, decode_rows_max=decode_rows_max)
     qpk = hq // hkv
-    rows_max = (2 ** 31 - 1) if decode_rows_max < 0 else decode_rows_max
+    # the prefill kernel takes bf16 caches with qpk dividing 128 (block size 16 here)
+    prefill_ok = 128 % qpk == 0
+    rows_max = (2 ** 63) if not prefill_ok else (32 if decode_rows_max < 0 else decode_rows_max)
     seen = {}
     for kind, tiles, rows_per in (("pre", pre, 128), ("dec", dec, 8)):
         for t in tiles:
@@ -135,7 +137,8 @@ def _check_schedule(cu, kv, hq, hkv, causal=1, window=0, num_splits=0, num_sms=1
             bounds[bkey] = (vmin, vmax)
         vmin, vmax = bounds[bkey]
         assert hi == vmax + 1
-        assert lo == (vmin // 16) * 16
+        align = 16 if kind == "dec" else 128
+        assert lo == (vmin // align) * align
         assert lo % 16 == 0 and all(p[0] % 16 == 0 for p in pieces)
         assert hi <= kv[s]
         if len(owners) > 1:

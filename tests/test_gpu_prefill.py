@@ -1,0 +1,139 @@
+"""GPU parity of the tcgen05 prefill path (through the C ABI) against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_attention_unified_gb300 as ua
+from paged_kv_attention_unified_gb300 import torch_utils as tu
+import workloads as W
+
+from _helpers import as_f64, assert_close, oracle_full, oracle_rows, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_attention_unified_gb300 import build
+    build.build()
+
+
+def _check(case, decode_rows_max=0, num_splits=0):
+    """decode_rows_max=0 sends every sequence the prefill kernel can take to it."""
+    b = tu.to_device(case)
+    with tu.make_plan(b, num_splits=num_splits, decode_rows_max=decode_rows_max) as plan:
+        assert plan.info.num_prefill_tiles > 0
+        out = tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    return assert_close(as_f64(out), oracle_full(case), case.kv_dtype, case.name)
+
+
+def test_single_tile_prefill():
+    _check(W.make_case("one_tile", [100], [100], 1, 1, 128, 16, seed=1))
+
+
+def test_tiny_mixed_config_through_prefill():
+    _check(W.config1_tiny_mixed(), decode_rows_max=4)
+
+
+@pytest.mark.parametrize("qpk,hkv", [(1, 2), (2, 2), (4, 2), (8, 1), (16, 1)])
+def test_random_gqa(qpk, hkv):
+    _check(W.random_small_case(200 + qpk, head_dim=128, num_q_heads=qpk * hkv,
+                               num_kv_heads=hkv, max_kv=700, max_seqs=4))
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128, 256])
+def test_block_sizes(bs):
+    _check(W.make_case(f"bs{bs}", [300, 77, 1], [300, 500, 40], 8, 2, 128, bs, seed=bs))
+
+
+def test_head_dim_64():
+    _check(W.random_small_case(230, head_dim=64, num_q_heads=8, num_kv_heads=2, max_kv=800))
+    _check(W.make_case("d64_long", [700], [1500], 4, 4, 64, 16, seed=231))
+
+
+def test_window_and_noncausal():
+    _check(W.make_case("win", [400, 260], [900, 260], 8, 2, 128, 16, window=150, seed=240))
+    _check(W.make_case("win128", [300], [800], 4, 4, 128, 128, window=200, seed=241))
+    _check(W.make_case("noncausal", [200, 90], [600, 90], 8, 2, 128, 16, causal=False, seed=242))
+
+
+def test_nan_poisoned_padding_never_leaks():
+    _check(W.make_case("poison", [333, 150], [700, 181], 8, 2, 128, 16, poison=True, seed=250))
+    _check(W.make_case("poison128", [333], [459], 4, 4, 128, 128, poison=True, seed=251))
+
+
+def test_dense_causal_small():
+    _check(W.make_case("dense", [1024, 1024], [1024, 1024], 4, 4, 128, 128, table="identity",
+                       seed=260))
+
+
+def test_mixed_prefill_and_decode_in_one_plan():
+    case = W.make_case("mixed", [1, 600, 1, 1, 37, 900], [3000, 1400, 70, 5000, 37, 900], 16, 4,
+                       128, 16, seed=270)
+    _check(case, decode_rows_max=32)
+
+
+def test_block_permutation_gives_identical_bits():
+    case = W.make_case("perm", [500, 200], [800, 333], 8, 2, 128, 16, seed=280)
+    b = tu.to_device(case)
+    with tu.make_plan(b, decode_rows_max=0) as plan:
+        a = tu.forward(plan, b).cpu()
+    nb = case.num_blocks
+    perm = torch.randperm(nb, generator=torch.Generator().manual_seed(3))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(nb)
+    k2, v2 = torch.empty_like(case.k_cache), torch.empty_like(case.v_cache)
+    k2[inv] = case.k_cache
+    v2[inv] = case.v_cache
+    case2 = W.Case(**{**case.__dict__, "k_cache": k2, "v_cache": v2,
+                      "block_tables": inv[case.block_tables.long()].to(torch.int32)})
+    b2 = tu.to_device(case2)
+    with tu.make_plan(b2, decode_rows_max=0) as plan:
+        c = tu.forward(plan, b2).cpu()
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_full_size_dense_prefill_sampled_and_first_row_exact():
+    """The dense causal prefill workload in the benchmark's launch
+    configuration: sampled rows against the oracle, and row 0 of every
+    (sequence, head) -- which sees key 0 alone -- equal to V[0] bit for bit."""
+    case = W.config4_dense_prefill()
+    got = tu.run(case)
+    rows = sample_rows(case, 24, seed=4)
+    exp = oracle_rows(case, rows)
+    assert_close(np.stack([as_f64(got[t, h]) for t, h in rows]), exp, case.kv_dtype, case.name)
+    for s in range(case.num_seqs):
+        page = int(case.block_tables[s, 0])
+        for h in range(case.num_q_heads):
+            assert torch.equal(got[4096 * s, h].view(torch.int16),
+                               case.v_cache[page, 0, h].view(torch.int16))
+
+
+def test_full_size_mixed_config_sampled():
+    case = W.config3_mixed()
+    got = tu.run(case)
+    rows = sample_rows(case, 32, seed=3)
+    exp = oracle_rows(case, rows)
+    assert_close(np.stack([as_f64(got[t, h]) for t, h in rows]), exp, case.kv_dtype, case.name)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """The producer is told to issue nothing: every consumer wait runs out
+    after 50 ms, the kernel records UA_ERR_DEVICE_TIMEOUT and exits; the same
+    plan then runs normally."""
+    case = W.make_case("timeout", [256], [256], 4, 4, 128, 16, seed=290)
+    b = tu.to_device(case)
+    with tu.make_plan(b, decode_rows_max=0) as plan:
+        ua.ua_plan_set_debug(plan.handle, 1, 50_000_000)
+        tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == ua.UA_ERR_DEVICE_TIMEOUT
+        ua.ua_plan_set_debug(plan.handle, 0, 0)
+        out = tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    assert_close(as_f64(out), oracle_full(case), W.BF16, "after timeout")
