@@ -163,7 +163,25 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
     return a.kv_lo < b.kv_lo;
   };
   std::stable_sort(s.decode.begin(), s.decode.end(), longer);
-  std::stable_sort(s.prefill.begin(), s.prefill.end(), longer);
+  // Prefill tiles stay grouped by (sequence, KV head), longest group first and
+  // longest tile first inside a group: CTAs running at the same time then read
+  // the same K/V rows, which stay in L2 (a head's K/V is a few MB; all heads
+  // at once would not fit).
+  {
+    std::vector<int64_t> group_work(static_cast<size_t>(p.num_seqs) * p.num_kv_heads, 0);
+    auto gi = [&](const ua_tile& t) {
+      return static_cast<size_t>(t.seq) * p.num_kv_heads + t.kv_head;
+    };
+    for (const ua_tile& t : s.prefill)
+      group_work[gi(t)] += static_cast<int64_t>(t.kv_hi - t.kv_lo) * t.nrows;
+    std::stable_sort(s.prefill.begin(), s.prefill.end(),
+                     [&](const ua_tile& a, const ua_tile& b) {
+                       const int64_t ga = group_work[gi(a)], gb = group_work[gi(b)];
+                       if (ga != gb) return ga > gb;
+                       if (gi(a) != gi(b)) return gi(a) < gi(b);
+                       return longer(a, b);
+                     });
+  }
   *out = std::move(s);
   return UA_OK;
 }

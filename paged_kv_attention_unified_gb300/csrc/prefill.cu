@@ -36,13 +36,17 @@ using namespace sm100;
 
 constexpr int kRows = 128;       // query rows per tile (TMEM lanes, MMA M)
 constexpr int kKeys = 128;       // keys per key tile (MMA N of S, K of PV)
-constexpr int kStages = 2;       // K/V ring depth
 constexpr int kThreads = 192;    // 6 warps
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
+// K/V ring depth: as deep as 227 KB of shared memory allows.
+template <int D>
+constexpr int stages_for() { return D == 128 ? 3 : 4; }
+
 template <int D>
 struct Smem {
+  static constexpr int kStages = stages_for<D>();
   static constexpr int kPanel = kRows * 128;           // one 64-wide bf16 panel: 16 KB
   static constexpr int kTile = kRows * D * 2;           // 128 x D bf16
   static constexpr int kQ = 0;
@@ -67,6 +71,7 @@ struct Bars {
   uint64_t* mma_done;
 };
 
+template <int kStages>
 __device__ __forceinline__ Bars bars_at(uint64_t* b) {
   Bars r;
   r.q_full = b;
@@ -96,6 +101,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CU
                                               volatile int32_t* abort, volatile int32_t* never) {
   using L = Smem<D>;
   constexpr int kPanels = D / 64;
+  constexpr int kStages = L::kStages;
   prefetch_tmap(map_q);
   prefetch_tmap(map_k);
   prefetch_tmap(map_v);
@@ -161,6 +167,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, int n_tiles, ui
                                          const Bars& bar, volatile int32_t* abort,
                                          volatile int32_t* never) {
   using L = Smem<D>;
+  constexpr int kStages = L::kStages;
   constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);
   constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 0, 1);
   const uint32_t tmem_o = tmem + 256;
@@ -226,6 +233,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const ua_ti
                                              int lane) {
   using L = Smem<D>;
   constexpr int kPanels = D / 64;
+  constexpr int kStages = L::kStages;
   const uint32_t tmem_o = tmem + 256;
   const int quarter = warp & 3;
   const int r = quarter * 32 + lane;
@@ -367,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = sm + L::kQ;
   uint8_t* sK = sm + L::kK;
   uint8_t* sV = sm + L::kV;
-  const Bars bar = bars_at(reinterpret_cast<uint64_t*>(sm + L::kBar));
+  constexpr int kStages = L::kStages;
+  const Bars bar = bars_at<kStages>(reinterpret_cast<uint64_t*>(sm + L::kBar));
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc);
   volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(sm + L::kMisc + 8);
   volatile int32_t* never = reinterpret_cast<volatile int32_t*>(sm + L::kMisc + 12);
