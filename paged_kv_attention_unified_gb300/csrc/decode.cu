@@ -22,7 +22,10 @@
 // Online softmax in base 2 ("Fused Attention" notes, _attn_fwd_inner): running
 // max m, running sum l, rescale factor 2^(m_old - m_new).
 // Four warps per CTA take interleaved 16-key steps of the tile's range and
-// merge their (m, l, O) through shared memory at the end.
+// merge their (m, l, O) through shared memory at the end. A split piece
+// leaves its normalised partial and base-2 lse in the workspace; with arrival
+// counters given, the last piece of a group to finish merges the group in the
+// same launch (otherwise the combine kernel does).
 #include "ua_device.cuh"
 #include "ua_kernels.h"
 
@@ -398,30 +401,32 @@ __global__ void __launch_bounds__(kThreads)
   constexpr int kSeg = D / 16;  // dims per thread in the epilogue
   const int n = threadIdx.x / 16;
   const int d0 = (threadIdx.x % 16) * kSeg;
-  if (n >= nrows) return;
-  float M = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][n]);
-  float L = 0.f;
+  const bool row_ok = n < nrows;
+  float M = -INFINITY, L = 0.f;
   float o[kSeg];
 #pragma unroll
   for (int e = 0; e < kSeg; ++e) o[e] = 0.f;
+  if (row_ok) {
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const float mw = red_m[w][n];
-    const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-    L += f * red_l[w][n];
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, red_m[w][n]);
 #pragma unroll
-    for (int e = 0; e < kSeg; ++e) o[e] += f * red_acc[w][n][d0 + e];
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = red_m[w][n];
+      const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+      L += f * red_l[w][n];
+#pragma unroll
+      for (int e = 0; e < kSeg; ++e) o[e] += f * red_acc[w][n][d0 + e];
+    }
   }
-  const float inv = L > 0.f ? p.v_scale / L : 0.f;
-  if (tile.slot < 0) {
+  // bf16 output row n of this tile, scaled by `mult`.
+  auto store_out = [&](const float* vals, float mult) {
     const int r = tile.row0 + n;
     const int tok = q_start + r / p.qpk;
     const int head = tile.kv_head * p.qpk + r % p.qpk;
     uint32_t packed[kSeg / 2];
 #pragma unroll
-    for (int e = 0; e < kSeg / 2; ++e) packed[e] = pack2<false>(o[2 * e] * inv, o[2 * e + 1] * inv);
+    for (int e = 0; e < kSeg / 2; ++e)
+      packed[e] = pack2<false>(vals[2 * e] * mult, vals[2 * e + 1] * mult);
     uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) +
                    ((static_cast<int64_t>(tok) * p.num_q_heads + head) * D + d0) * 2;
     if constexpr (kSeg == 8) {
@@ -429,7 +434,14 @@ __global__ void __launch_bounds__(kThreads)
     } else {
       *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
     }
-  } else {
+  };
+  const float inv = L > 0.f ? p.v_scale / L : 0.f;
+  if (tile.slot < 0) {
+    if (row_ok) store_out(o, inv);
+    return;
+  }
+  // Split piece: normalised partial row and its base-2 log-sum-exp.
+  if (row_ok) {
     float* wo = p.ws_o + (static_cast<int64_t>(tile.slot) * UA_DECODE_ROWS + n) * D + d0;
 #pragma unroll
     for (int e = 0; e < kSeg; e += 4)
@@ -439,6 +451,47 @@ __global__ void __launch_bounds__(kThreads)
       p.ws_lse[static_cast<int64_t>(tile.slot) * UA_DECODE_ROWS + n] =
           L > 0.f ? M + log2f(L) : -INFINITY;
   }
+  if (p.split_counters == nullptr) return;  // a separate combine kernel merges the pieces
+  // Fused combine: the last piece of a group to finish merges all of them
+  // (weights 2^(lse_s - lse*)), then re-arms the group's counter for the next call.
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int ns = p.groups[tile.group].nsplits;
+    s_last = atomicAdd(&p.split_counters[tile.group], 1) == ns - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const ua_combine_group grp = p.groups[tile.group];
+  if (row_ok) {
+    const float* lse = p.ws_lse + static_cast<int64_t>(grp.slot0) * UA_DECODE_ROWS + n;
+    float Mx = -INFINITY;
+    for (int sp = 0; sp < grp.nsplits; ++sp) Mx = fmaxf(Mx, __ldcg(lse + sp * UA_DECODE_ROWS));
+    float W = 0.f;
+    float acc[kSeg];
+#pragma unroll
+    for (int e = 0; e < kSeg; ++e) acc[e] = 0.f;
+    for (int sp = 0; sp < grp.nsplits; ++sp) {
+      const float l = __ldcg(lse + sp * UA_DECODE_ROWS);
+      if (l == -INFINITY) continue;
+      const float w = ex2(l - Mx);
+      W += w;
+      const float* src =
+          p.ws_o + ((static_cast<int64_t>(grp.slot0) + sp) * UA_DECODE_ROWS + n) * D + d0;
+#pragma unroll
+      for (int e = 0; e < kSeg; e += 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + e));
+        acc[e] += w * v.x;
+        acc[e + 1] += w * v.y;
+        acc[e + 2] += w * v.z;
+        acc[e + 3] += w * v.w;
+      }
+    }
+    store_out(acc, W > 0.f ? 1.f / W : 0.f);
+  }
+  if (threadIdx.x == 0) p.split_counters[tile.group] = 0;
 }
 
 }  // namespace

@@ -250,13 +250,15 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const ua_ti
     const int base = kv_lo + j * kKeys;
     const uint32_t s_tmem = tmem + lane_addr + (j & 1) * kKeys;
     float x[kKeys];
+    {
+      uint32_t v[kKeys / 32][32];
 #pragma unroll
-    for (int ch = 0; ch < kKeys / 32; ++ch) {
-      uint32_t v[32];
-      tmem_ld32(s_tmem + ch * 32, v);
+      for (int ch = 0; ch < kKeys / 32; ++ch) tmem_ld32(s_tmem + ch * 32, v[ch]);
       tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 32; ++i) x[ch * 32 + i] = __uint_as_float(v[i]) * c;
+      for (int ch = 0; ch < kKeys / 32; ++ch)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[ch * 32 + i] = __uint_as_float(v[ch][i]) * c;
     }
     // Mask by select: keys past the range, past the row's position (causal)
     // or at or below pos - window.
@@ -267,22 +269,38 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const ua_ti
       for (int i = 0; i < kKeys; ++i)
         if (i >= hi_col || i < lo_col) x[i] = -INFINITY;
     }
-    float mx = x[0];
+    // Row max with independent partial maxima (no 128-long dependency chain).
+    constexpr int kAcc = 8;
+    float mxp[kAcc];
 #pragma unroll
-    for (int i = 1; i < kKeys; ++i) mx = fmaxf(mx, x[i]);
+    for (int a = 0; a < kAcc; ++a) mxp[a] = x[a];
+#pragma unroll
+    for (int i = kAcc; i < kKeys; ++i) mxp[i % kAcc] = fmaxf(mxp[i % kAcc], x[i]);
+#pragma unroll
+    for (int w = kAcc / 2; w > 0; w /= 2)
+#pragma unroll
+      for (int a = 0; a < w; ++a) mxp[a] = fmaxf(mxp[a], mxp[a + w]);
+    const float mx = mxp[0];
     const float m_new = fmaxf(m, mx);
     const bool grow = (m == -INFINITY) || (m_new > m + kRescaleThreshold);
     const float m_use = grow ? m_new : m;
     const float alpha = grow ? ((m == -INFINITY) ? 0.f : ex2(m - m_use)) : 1.f;
     const float sub = (m_use == -INFINITY) ? 0.f : m_use;
-    float rowsum = 0.f;
+    float sump[kAcc];
+#pragma unroll
+    for (int a = 0; a < kAcc; ++a) sump[a] = 0.f;
     uint32_t pk[kKeys / 2];
 #pragma unroll
     for (int i = 0; i < kKeys / 2; ++i) {
       const float p0 = ex2(x[2 * i] - sub), p1 = ex2(x[2 * i + 1] - sub);
-      rowsum += p0 + p1;
+      sump[i % kAcc] += p0 + p1;
       pk[i] = pack2<false>(p0, p1);
     }
+#pragma unroll
+    for (int w = kAcc / 2; w > 0; w /= 2)
+#pragma unroll
+      for (int a = 0; a < w; ++a) sump[a] += sump[a + w];
+    const float rowsum = sump[0];
     l = l * alpha + rowsum;
     m = m_use;
     // Rescale O in TMEM when some row of this warp moved its max.

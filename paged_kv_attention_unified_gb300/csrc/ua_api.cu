@@ -23,6 +23,7 @@ struct ua_plan {
   ua_tile* d_decode = nullptr;
   ua_combine_group* d_groups = nullptr;
   int32_t* d_err = nullptr;
+  int32_t* d_counters = nullptr;   // per combine group, zero between calls
   float* d_ws = nullptr;           // split workspace: partial rows then lse values
   float* d_ws_o = nullptr;
   float* d_ws_lse = nullptr;
@@ -232,7 +233,7 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   const size_t n_pre = s.prefill.size(), n_dec = s.decode.size(), n_grp = s.groups.size();
   const size_t bytes_tiles = (n_pre + n_dec) * sizeof(ua_tile);
   const size_t bytes_groups = n_grp * sizeof(ua_combine_group);
-  const size_t bytes_meta = bytes_tiles + bytes_groups + 16;
+  const size_t bytes_meta = bytes_tiles + bytes_groups + 16 + n_grp * sizeof(int32_t);
   std::vector<uint8_t> host(bytes_meta, 0);
   if (n_pre) std::memcpy(host.data(), s.prefill.data(), n_pre * sizeof(ua_tile));
   if (n_dec) std::memcpy(host.data() + n_pre * sizeof(ua_tile), s.decode.data(),
@@ -249,6 +250,7 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   plan->d_decode = reinterpret_cast<ua_tile*>(base + n_pre * sizeof(ua_tile));
   plan->d_groups = reinterpret_cast<ua_combine_group*>(base + bytes_tiles);
   plan->d_err = reinterpret_cast<int32_t*>(base + bytes_tiles + bytes_groups);
+  plan->d_counters = reinterpret_cast<int32_t*>(base + bytes_tiles + bytes_groups + 16);
   if (plan->info.workspace_bytes > 0) {
     if (cudaMalloc(&plan->d_ws, static_cast<size_t>(plan->info.workspace_bytes)) != cudaSuccess) {
       free_plan_memory(plan);
@@ -354,23 +356,12 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
   if (!s.decode.empty()) {
     kp.tiles = plan->d_decode;
     kp.num_tiles = static_cast<int32_t>(s.decode.size());
+    // split pieces are merged inside the decode launch (last piece per group)
+    kp.split_counters = s.groups.empty() ? nullptr : plan->d_counters;
+    kp.groups = plan->d_groups;
     auto* ev = timing_begin(mp, 1, cs);
     if (ua::launch_decode(kp, plan->prob.head_dim, plan->prob.kv_dtype, cs) != cudaSuccess)
       return UA_ERR_CUDA;
-    timing_end(ev, cs);
-  }
-  if (!s.groups.empty()) {
-    ua::CombineParams cp;
-    cp.groups = plan->d_groups;
-    cp.num_groups = static_cast<int32_t>(s.groups.size());
-    cp.ws_o = plan->d_ws_o;
-    cp.ws_lse = plan->d_ws_lse;
-    cp.cu_query_lens = cu_query_lens;
-    cp.out = out;
-    cp.num_q_heads = plan->prob.num_q_heads;
-    cp.qpk = plan->prob.num_q_heads / plan->prob.num_kv_heads;
-    auto* ev = timing_begin(mp, 2, cs);
-    if (ua::launch_combine(cp, plan->prob.head_dim, cs) != cudaSuccess) return UA_ERR_CUDA;
     timing_end(ev, cs);
   }
   return UA_OK;

@@ -38,6 +38,10 @@ struct KernelParams {
   int32_t window;
   float score_scale_log2;  // scale * log2(e) (* k_scale for fp8)
   float v_scale;           // 1 for bf16
+  // Fused split combine: per-group arrival counters (zero between calls) and
+  // the groups; null counters leave the merge to the combine kernel.
+  int32_t* split_counters;
+  const ua_combine_group* groups;
 };
 
 struct CombineParams {
