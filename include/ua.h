@@ -84,7 +84,7 @@ typedef struct {
   int32_t seq;      /* sequence index */
   int32_t kv_head;  /* KV head g */
   int32_t row0;     /* first packed row of this tile */
-  int32_t nrows;    /* rows in this tile (<= 8 decode, <= 128 prefill) */
+  int32_t nrows;    /* rows in this tile (<= 8 decode, <= 256 prefill) */
   int32_t kv_lo;    /* first key position this tile reads */
   int32_t kv_hi;    /* one past the last key position this tile reads */
   int32_t slot;     /* split workspace slot, or -1: write the output directly */
@@ -102,7 +102,7 @@ typedef struct {
 
 #define UA_MAX_SPLITS 128
 #define UA_DECODE_ROWS 8     /* rows of one decode tile */
-#define UA_PREFILL_ROWS 128  /* rows of one prefill tile (tcgen05 M) */
+#define UA_PREFILL_ROWS 256  /* rows of one prefill tile: two tcgen05 M=128 query tiles */
 
 typedef struct {
   int64_t num_prefill_tiles;

@@ -26,7 +26,7 @@ UA_KV_BF16 = 0
 UA_KV_FP8_E4M3 = 1
 UA_MAX_SPLITS = 128
 UA_DECODE_ROWS = 8
-UA_PREFILL_ROWS = 128
+UA_PREFILL_ROWS = 256
 
 # Every symbol include/ua.h declares.
 EXPORTS = (

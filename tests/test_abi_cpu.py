@@ -99,7 +99,7 @@ def _check_schedule(cu, kv, hq, hkv, causal=1, window=0, num_splits=0, num_sms=1
     prefill_ok = 128 % qpk == 0
     rows_max = (2 ** 63) if not prefill_ok else (32 if decode_rows_max < 0 else decode_rows_max)
     seen = {}
-    for kind, tiles, rows_per in (("pre", pre, 128), ("dec", dec, 8)):
+    for kind, tiles, rows_per in (("pre", pre, ua.UA_PREFILL_ROWS), ("dec", dec, 8)):
         for t in tiles:
             assert 1 <= t["nrows"] <= rows_per
             for r in range(t["row0"], t["row0"] + t["nrows"]):
