@@ -10,14 +10,14 @@
 // query tiles are interleaved on the tensor core in the ping-pong manner the
 // notes describe for FlashAttention-3, so that one tile's softmax overlaps
 // the other tile's matrix products:
-//   warp 0      TMA producer: lane 0 loads Q (both tiles) and K pages into a
-//               K ring, lane 1 loads V pages into a V ring (one box per page,
-//               resolved through the block table);
+//   warp 0      TMA producer of Q (both tiles) and of the K ring, and
+//   warp 2      TMA producer of the V ring (one box per page, resolved through
+//               the block table);
 //   warp 1      owns the tensor memory; one thread issues the MMAs in the order
 //               S0(j) S1(j) | PV0(j) S0(j+1) | PV1(j) S1(j+1) | ...
 //               (S_t into TMEM columns 128t, O_t into 256 + 128t; P_t is read
 //               from TMEM where the softmax wrote it over S_t);
-//   warps 2-3   idle (they complete the control warpgroup);
+//   warp 3      idle (it completes the control warpgroup);
 //   warps 4-7   softmax of query tile 0, one row per thread (TMEM lane);
 //   warps 8-11  softmax of query tile 1.
 // Softmax: scale, mask by select, running max / sum, P = 2^(x - m) stored as
@@ -111,7 +111,8 @@ __device__ __forceinline__ void give_up(const PrefillParams& p, volatile int32_t
 }
 
 // ------------------------------------------------------------------ producer
-// Lane 0 of warp 0: Q of both query tiles, then the K ring. Lane 1: the V ring.
+// One thread of warp 0: Q of both query tiles, then the K ring. One thread of
+// warp 2: the V ring.
 // Every page id is read from the block table and checked; a missing or
 // out-of-range page is loaded from an out-of-range block coordinate, which
 // TMA fills with zeros.
@@ -498,13 +499,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     if (g.nmax > 0) {
-      if (warp == 0) {
-        if (lane == 0)
-          producer_role<D, false>(&map_q, &map_k, p, tile, g, sQ, sK, bar.kfull, bar.kempty, KS,
-                                  bar.q_full, abort, never);
-        else if (lane == 1)
-          producer_role<D, true>(&map_q, &map_v, p, tile, g, sQ, sV, bar.vfull, bar.vempty, VS,
-                                 bar.q_full, abort, never);
+      if (warp == 0 && lane == 0) {
+        producer_role<D, false>(&map_q, &map_k, p, tile, g, sQ, sK, bar.kfull, bar.kempty, KS,
+                                bar.q_full, abort, never);
+      } else if (warp == 2 && lane == 0) {
+        producer_role<D, true>(&map_q, &map_v, p, tile, g, sQ, sV, bar.vfull, bar.vempty, VS,
+                               bar.q_full, abort, never);
       } else if (warp == 1 && lane == 0) {
         mma_role<D>(p, g, sQ, sK, sV, tmem, bar, abort, never);
       }
