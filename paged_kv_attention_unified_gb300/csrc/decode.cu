@@ -26,6 +26,7 @@
 // leaves its normalised partial and base-2 lse in the workspace; with arrival
 // counters given, the last piece of a group to finish merges the group in the
 // same launch (otherwise the combine kernel does).
+#include "sm100.cuh"
 #include "ua_device.cuh"
 #include "ua_kernels.h"
 
@@ -78,24 +79,23 @@ struct StepRegs {
   uint32_t v[4][DecodeCfg<D, FP8>::VW];   // V rows 4t .. 4t+3
 };
 
-// Issue the loads of one 16-key step starting at key `base` of page `page`
-// (-1: nothing readable). Keys at or beyond kv_hi read as zero.
+// Registers of one 16-key step from its shared-memory stage: kp / vp hold the
+// step's K and V rows (16 rows of head_dim elements, as the TMA box lands).
+// Keys at or beyond kv_hi read as zero (the page may hold anything there).
 template <int D, bool FP8>
-__device__ __forceinline__ void load_step(StepRegs<D, FP8>& r, const KernelParams& p,
-                                          const uint8_t* kc, const uint8_t* vc, int base,
-                                          int64_t page, int kv_hi, int kv_head, int g, int t) {
+__device__ __forceinline__ void read_step(StepRegs<D, FP8>& r, const uint8_t* kp,
+                                          const uint8_t* vp, int base, int kv_hi, int g, int t) {
   using C = DecodeCfg<D, FP8>;
-  const int slot0 = base % p.block_size;
+  constexpr int kRowBytes = D * C::ELT;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int key = key_of_row(g + 8 * h);
-    const bool ok = page >= 0 && base + key < kv_hi;
-    const uint8_t* row =
-        kc + (kv_row_offset(p, page < 0 ? 0 : page, slot0 + key, kv_head, D)) * C::ELT;
+    const bool ok = base + key < kv_hi;
+    const uint8_t* row = kp + key * kRowBytes;
 #pragma unroll
     for (int l = 0; l < C::NKL; ++l) {
       uint4 x = make_uint4(0u, 0u, 0u, 0u);
-      if (ok) x = ld_stream_v4(row + (l * 4 * C::KE + t * C::KE) * C::ELT);
+      if (ok) x = *reinterpret_cast<const uint4*>(row + (l * 4 * C::KE + t * C::KE) * C::ELT);
       r.k[h][4 * l + 0] = x.x;
       r.k[h][4 * l + 1] = x.y;
       r.k[h][4 * l + 2] = x.z;
@@ -105,22 +105,21 @@ __device__ __forceinline__ void load_step(StepRegs<D, FP8>& r, const KernelParam
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int key = 4 * t + j;
-    const bool ok = page >= 0 && base + key < kv_hi;
-    const uint8_t* row =
-        vc + (kv_row_offset(p, page < 0 ? 0 : page, slot0 + key, kv_head, D)) * C::ELT;
+    const bool ok = base + key < kv_hi;
+    const uint8_t* row = vp + key * kRowBytes;
 #pragma unroll
     for (int l = 0; l < C::NVL; ++l) {
       const uint8_t* a = row + (l * 8 * C::VE + g * C::VE) * C::ELT;
       if constexpr (C::VLB == 16) {
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (ok) x = ld_stream_v4(a);
+        if (ok) x = *reinterpret_cast<const uint4*>(a);
         r.v[j][4 * l + 0] = x.x;
         r.v[j][4 * l + 1] = x.y;
         r.v[j][4 * l + 2] = x.z;
         r.v[j][4 * l + 3] = x.w;
       } else {
         uint2 x = make_uint2(0u, 0u);
-        if (ok) x = ld_stream_v2(a);
+        if (ok) x = *reinterpret_cast<const uint2*>(a);
         r.v[j][2 * l + 0] = x.x;
         r.v[j][2 * l + 1] = x.y;
       }
@@ -238,17 +237,50 @@ __device__ __forceinline__ void compute_step(WarpState<D>& st, const StepRegs<D,
   }
 }
 
+// Shared memory of one CTA: a ring of R stages per warp, each holding the K
+// and V rows (16 x head_dim) of one 16-key step as TMA lands them; then one
+// mbarrier per stage. After the loop the ring is reused for the cross-warp
+// merge. About 64 KB, so that three CTAs (twelve warps) share an SM.
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads)
-    decode_kernel(const KernelParams p) {
+struct Ring {
+  static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
+  static constexpr int kStage = 2 * 16 * kRowBytes;
+  static constexpr int kStages = kStage >= 8192 ? 2 : (kStage >= 4096 ? 4 : 8);
+  static constexpr int kRing = kWarps * kStages * kStage;
+  static constexpr int kBars = kRing;
+  static constexpr int kMisc = kBars + 8 * kWarps * kStages;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 128;  // slack for 128-byte alignment
+  static_assert(kWarps * UA_DECODE_ROWS * (D + 2) * 4 <= kRing, "merge buffers alias the ring");
+};
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(kThreads, 3)
+    decode_kernel(const __grid_constant__ CUtensorMap map_k,
+                  const __grid_constant__ CUtensorMap map_v, const KernelParams p) {
   using C = DecodeCfg<D, FP8>;
-  __shared__ float red_acc[kWarps][UA_DECODE_ROWS][D];
-  __shared__ float red_m[kWarps][UA_DECODE_ROWS];
-  __shared__ float red_l[kWarps][UA_DECODE_ROWS];
+  using RC = Ring<D, FP8>;
+  constexpr int R = RC::kStages;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t* dsm = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(dsm_raw) + 127) & ~static_cast<uintptr_t>(127));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + RC::kBars);
+  volatile int32_t* never = reinterpret_cast<volatile int32_t*>(dsm + RC::kMisc);
+  // merge buffers (valid only after the loop; they alias the ring)
+  float (*red_acc)[UA_DECODE_ROWS][D] = reinterpret_cast<float (*)[UA_DECODE_ROWS][D]>(dsm);
+  float (*red_m)[UA_DECODE_ROWS] =
+      reinterpret_cast<float (*)[UA_DECODE_ROWS]>(dsm + kWarps * UA_DECODE_ROWS * D * 4);
+  float (*red_l)[UA_DECODE_ROWS] = red_m + kWarps;
 
   const ua_tile tile = p.tiles[blockIdx.x];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
+  if (threadIdx.x == 0) {
+    *never = 0;
+    for (int i = 0; i < kWarps * R; ++i) sm100::mbar_init(&bars[i], 1);
+    sm100::fence_mbar_init();
+  }
+  __syncthreads();
 
   // Per-sequence values from the device arrays; every range is clamped so
   // that disagreeing host/device lengths cannot send a read out of bounds.
@@ -341,60 +373,98 @@ __global__ void __launch_bounds__(kThreads)
     mk.lo_full = p.window > 0 ? max_pos - p.window + 1 : INT_MIN;
   }
 
-  WarpState<D> st;
+  WarpState<D> st_state;
 #pragma unroll
   for (int c = 0; c < C::NC; ++c)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) st.acc[c][e] = 0.f;
-  st.m[0] = st.m[1] = -INFINITY;
-  st.l[0] = st.l[1] = 0.f;
+    for (int e = 0; e < 4; ++e) st_state.acc[c][e] = 0.f;
+  st_state.m[0] = st_state.m[1] = -INFINITY;
+  st_state.l[0] = st_state.l[1] = 0.f;
 
-  // ---- Stream the key range: warp w takes steps w, w+4, w+8, ...
-  const uint8_t* kc = reinterpret_cast<const uint8_t*>(p.k_cache);
-  const uint8_t* vc = reinterpret_cast<const uint8_t*>(p.v_cache);
+  // ---- Stream the key range: warp w takes steps w, w+4, w+8, ...; each step
+  // is one TMA box of K and one of V (16 keys of one page) into the warp's ring.
   const int nsteps = kv_hi > kv_lo ? (kv_hi - kv_lo + 15) / 16 : 0;
   const int my_n = nsteps > warp ? (nsteps - warp + kWarps - 1) / kWarps : 0;
   auto step_base = [&](int k) { return kv_lo + 16 * (warp + kWarps * k); };
-
-  StepRegs<D, FP8> ra, rb;
-  if (my_n > 0) {
-    int64_t pg_next = my_n > 1 ? page_of(p, tile.seq, step_base(1)) : -1;
-    load_step<D, FP8>(ra, p, kc, vc, step_base(0), page_of(p, tile.seq, step_base(0)), kv_hi,
-                      tile.kv_head, g, t);
-    for (int k = 0; k < my_n; k += 2) {
-      if (k + 1 < my_n)
-        load_step<D, FP8>(rb, p, kc, vc, step_base(k + 1), pg_next, kv_hi, tile.kv_head, g, t);
-      int64_t pg_n2 = k + 2 < my_n ? page_of(p, tile.seq, step_base(k + 2)) : -1;
-      compute_step<D, FP8>(st, ra, qb, cc, mk, step_base(k), g, t);
-      if (k + 1 >= my_n) break;
-      if (k + 2 < my_n)
-        load_step<D, FP8>(ra, p, kc, vc, step_base(k + 2), pg_n2, kv_hi, tile.kv_head, g, t);
-      pg_next = k + 3 < my_n ? page_of(p, tile.seq, step_base(k + 3)) : -1;
-      compute_step<D, FP8>(st, rb, qb, cc, mk, step_base(k + 1), g, t);
+  uint8_t* ring = dsm + warp * R * RC::kStage;
+  uint64_t* wbar = bars + warp * R;
+  // Page ids, 32 steps at a time: lane l holds the page of step 32c + l.
+  int32_t ids = -1;
+  auto refill_ids = [&](int c) {
+    const int k = 32 * c + lane;
+    ids = k < my_n ? p.block_tables[static_cast<int64_t>(tile.seq) * p.max_blocks_per_seq +
+                                    step_base(k) / p.block_size]
+                   : -1;
+  };
+  // Whole-warp call: every lane takes part in the shuffle, lane 0 issues.
+  auto issue = [&](int k) {
+    const int32_t id = __shfl_sync(0xffffffffu, ids, k & 31);
+    if (lane == 0) {
+      const int base = step_base(k);
+      int32_t blk = static_cast<int32_t>(p.num_blocks);  // out of range: TMA fills zeros
+      if (id >= 0 && static_cast<int64_t>(id) < p.num_blocks) blk = id;
+      else record_error(p.err, UA_ERR_BOUNDS);
+      const int st = k % R;
+      uint8_t* stage = ring + st * RC::kStage;
+      sm100::fence_proxy_async_smem();
+      sm100::mbar_arrive_expect_tx(&wbar[st], RC::kStage);
+      sm100::tma_load_4d(stage, &map_k, &wbar[st], 0, tile.kv_head, base % p.block_size, blk);
+      sm100::tma_load_4d(stage + 16 * RC::kRowBytes, &map_v, &wbar[st], 0, tile.kv_head,
+                         base % p.block_size, blk);
     }
+  };
+  int issued = 0, done = 0;
+  if (my_n > 0) {
+    refill_ids(0);
+    for (; issued < my_n && issued < R; ++issued) issue(issued);
+    StepRegs<D, FP8> r;
+    for (; done < my_n; ++done) {
+      const int st = done % R;
+      const bool ok = __all_sync(0xffffffffu, sm100::mbar_wait(&wbar[st], (done / R) & 1, never,
+                                                                p.timeout_ns));
+      if (!ok) {
+        record_error(p.err, UA_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+      const uint8_t* stage = ring + st * RC::kStage;
+      read_step<D, FP8>(r, stage, stage + 16 * RC::kRowBytes, step_base(done), kv_hi, g, t);
+      compute_step<D, FP8>(st_state, r, qb, cc, mk, step_base(done), g, t);
+      __syncwarp();  // every lane has consumed the stage: it may be refilled
+      if (issued < my_n) {
+        if ((issued & 31) == 0) refill_ids(issued >> 5);
+        issue(issued);
+        ++issued;
+      }
+    }
+    // Copies still in flight (only after a timeout) complete before exit.
+    if (lane == 0)
+      for (int k = done; k < issued; ++k)
+        sm100::mbar_wait(&wbar[k % R], (k / R) & 1, never, p.timeout_ns);
+    __syncwarp();
   }
+  __syncthreads();  // the ring is reused for the merge below
 
   // ---- Merge the four warps.
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
-    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 4);
-    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 8);
-    st.l[j] += __shfl_xor_sync(0xffffffffu, st.l[j], 16);
+    st_state.l[j] += __shfl_xor_sync(0xffffffffu, st_state.l[j], 4);
+    st_state.l[j] += __shfl_xor_sync(0xffffffffu, st_state.l[j], 8);
+    st_state.l[j] += __shfl_xor_sync(0xffffffffu, st_state.l[j], 16);
   }
   if (g == 0) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      red_m[warp][2 * t + j] = st.m[j];
-      red_l[warp][2 * t + j] = st.l[j];
+      red_m[warp][2 * t + j] = st_state.m[j];
+      red_l[warp][2 * t + j] = st_state.l[j];
     }
   }
 #pragma unroll
   for (int c = 0; c < C::NC; ++c) {
     const int d0 = v_dim<D, FP8>(2 * c, g);
-    red_acc[warp][2 * t][d0] = st.acc[c][0];
-    red_acc[warp][2 * t + 1][d0] = st.acc[c][1];
-    red_acc[warp][2 * t][d0 + 1] = st.acc[c][2];
-    red_acc[warp][2 * t + 1][d0 + 1] = st.acc[c][3];
+    red_acc[warp][2 * t][d0] = st_state.acc[c][0];
+    red_acc[warp][2 * t + 1][d0] = st_state.acc[c][1];
+    red_acc[warp][2 * t][d0 + 1] = st_state.acc[c][2];
+    red_acc[warp][2 * t + 1][d0 + 1] = st_state.acc[c][3];
   }
   __syncthreads();
 
@@ -494,19 +564,33 @@ __global__ void __launch_bounds__(kThreads)
   if (threadIdx.x == 0) p.split_counters[tile.group] = 0;
 }
 
+template <int D, bool FP8>
+cudaError_t launch_decode_d(const KernelParams& p, cudaStream_t stream) {
+  CUtensorMap mk, mv;
+  const int elt = FP8 ? 1 : 2;
+  // one box = the 16 key rows (all head dims) of one KV head in one page
+  cudaError_t e = encode_kv_page_map(&mk, p.k_cache, elt, D, p.num_kv_heads, p.block_size,
+                                     p.num_blocks, D, 16, false);
+  if (e == cudaSuccess)
+    e = encode_kv_page_map(&mv, p.v_cache, elt, D, p.num_kv_heads, p.block_size, p.num_blocks, D,
+                           16, false);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Ring<D, FP8>::kAlloc);
+  if (e != cudaSuccess) return e;
+  decode_kernel<D, FP8><<<p.num_tiles, kThreads, Ring<D, FP8>::kAlloc, stream>>>(mk, mv, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cudaStream_t stream) {
   if (p.num_tiles <= 0) return cudaSuccess;
-  const dim3 grid(p.num_tiles), block(kThreads);
-  if (kv_dtype == UA_KV_BF16) {
-    if (head_dim == 128) decode_kernel<128, false><<<grid, block, 0, stream>>>(p);
-    else decode_kernel<64, false><<<grid, block, 0, stream>>>(p);
-  } else {
-    if (head_dim == 128) decode_kernel<128, true><<<grid, block, 0, stream>>>(p);
-    else decode_kernel<64, true><<<grid, block, 0, stream>>>(p);
-  }
-  return cudaGetLastError();
+  if (kv_dtype == UA_KV_BF16)
+    return head_dim == 128 ? launch_decode_d<128, false>(p, stream)
+                           : launch_decode_d<64, false>(p, stream);
+  return head_dim == 128 ? launch_decode_d<128, true>(p, stream)
+                         : launch_decode_d<64, true>(p, stream);
 }
 
 }  // namespace ua

@@ -27,7 +27,6 @@
 // UA_ERR_DEVICE_TIMEOUT, makes the other roles give up, drains the copies and
 // MMAs in flight and frees the tensor memory before the CTA exits.
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include "sm100.cuh"
 #include "ua_device.cuh"
@@ -521,19 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  }
-  return fn;
-}
-
 template <int D>
 cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                      const PrefillParams& p, cudaStream_t stream) {
@@ -567,45 +553,24 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_
                            const void* v_cache, int64_t total_q, int head_dim, int num_kv_heads,
                            cudaStream_t stream) {
   if (p.num_tiles <= 0) return cudaSuccess;
-  auto encode = encode_fn();
-  if (encode == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t D = static_cast<cuuint64_t>(head_dim);
   CUtensorMap mq, mk, mv;
   {
     // Q as [total_q][Hq][D]: a box of (64 dims, qpk heads, 128/qpk tokens)
     // lands as 128 packed rows (token-major, head-minor) in one panel.
-    cuuint64_t dims[3] = {D, static_cast<cuuint64_t>(p.num_q_heads),
-                          static_cast<cuuint64_t>(total_q)};
-    cuuint64_t strides[2] = {D * 2, static_cast<cuuint64_t>(p.num_q_heads) * D * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(p.qpk),
-                         static_cast<cuuint32_t>(kRows / p.qpk)};
-    cuuint32_t es[3] = {1, 1, 1};
-    if (encode(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
-               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-        CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
+    const uint64_t D = static_cast<uint64_t>(head_dim);
+    uint64_t dims[3] = {D, static_cast<uint64_t>(p.num_q_heads), static_cast<uint64_t>(total_q)};
+    uint64_t strides[2] = {D * 2, static_cast<uint64_t>(p.num_q_heads) * D * 2};
+    uint32_t box[3] = {64, static_cast<uint32_t>(p.qpk), static_cast<uint32_t>(kRows / p.qpk)};
+    cudaError_t e = encode_tiled_map(&mq, 2, 3, q, dims, strides, box, true, false);
+    if (e != cudaSuccess) return e;
   }
-  {
-    // K/V cache as [num_blocks][block_size][Hkv][D]: one box = (64 dims, one
-    // head, rows_per_box slots, one block); an out-of-range block coordinate
-    // reads zeros.
-    cuuint64_t dims[4] = {D, static_cast<cuuint64_t>(num_kv_heads),
-                          static_cast<cuuint64_t>(p.block_size),
-                          static_cast<cuuint64_t>(p.num_blocks)};
-    cuuint64_t strides[3] = {D * 2, static_cast<cuuint64_t>(num_kv_heads) * D * 2,
-                             static_cast<cuuint64_t>(p.block_size) * num_kv_heads * D * 2};
-    cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(p.rows_per_box), 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    for (int which = 0; which < 2; ++which) {
-      void* base = const_cast<void*>(which == 0 ? k_cache : v_cache);
-      if (encode(which == 0 ? &mk : &mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims,
-                 strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) !=
-          CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    }
-  }
+  // K/V pages: (64 dims, one head, rows_per_box slots, one block) per box.
+  cudaError_t e = encode_kv_page_map(&mk, k_cache, 2, head_dim, num_kv_heads, p.block_size,
+                                     p.num_blocks, 64, p.rows_per_box, true);
+  if (e == cudaSuccess)
+    e = encode_kv_page_map(&mv, v_cache, 2, head_dim, num_kv_heads, p.block_size, p.num_blocks,
+                           64, p.rows_per_box, true);
+  if (e != cudaSuccess) return e;
   return head_dim == 128 ? launch_d<128>(mq, mk, mv, p, stream)
                          : launch_d<64>(mq, mk, mv, p, stream);
 }

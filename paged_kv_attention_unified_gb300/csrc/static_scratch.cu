@@ -150,7 +150,7 @@ extern "C" ua_status ua_forward_static_scratch(
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size < max_kv) return UA_ERR_INVALID_ARG;
   if (num_seqs == 0 || max_q == 0) return UA_OK;
   if (!q || !k_cache || !v_cache || !out || !cu_query_lens || !kv_lens || !block_tables ||
-      num_blocks <= 0)
+      num_blocks <= 0 || num_blocks >= INT32_MAX)
     return UA_ERR_INVALID_ARG;
   auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
   if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
@@ -215,6 +215,7 @@ extern "C" ua_status ua_forward_static_scratch(
   const bool fp8 = kv_dtype == UA_KV_FP8_E4M3;
   kp.score_scale_log2 = scale * kLog2e * (fp8 ? k_scale : 1.f);
   kp.v_scale = fp8 ? v_scale : 1.f;
+  kp.timeout_ns = 2000000000ull;
   if (launch_decode(kp, head_dim, kv_dtype, cs) != cudaSuccess) return UA_ERR_CUDA;
   if (splits > 1) {
     CombineParams cp;

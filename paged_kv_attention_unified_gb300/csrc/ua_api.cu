@@ -120,6 +120,7 @@ ua::KernelParams base_params(const ua_plan* plan, const void* q, const void* k, 
   const bool fp8 = pr.kv_dtype == UA_KV_FP8_E4M3;
   kp.score_scale_log2 = scale * ua::kLog2e * (fp8 ? k_scale : 1.f);
   kp.v_scale = fp8 ? v_scale : 1.f;
+  kp.timeout_ns = plan->wait_timeout_ns;
   return kp;
 }
 
@@ -319,7 +320,7 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return UA_ERR_CUDA;
   if (dev != plan->device) return UA_ERR_INVALID_ARG;
-  if (!s.prefill.empty() && num_blocks >= INT32_MAX) return UA_ERR_INVALID_ARG;  // TMA coordinate
+  if (num_blocks >= INT32_MAX) return UA_ERR_INVALID_ARG;  // TMA block coordinates are int32
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   ua_plan* mp = const_cast<ua_plan*>(plan);

@@ -42,6 +42,7 @@ struct KernelParams {
   // the groups; null counters leave the merge to the combine kernel.
   int32_t* split_counters;
   const ua_combine_group* groups;
+  uint64_t timeout_ns;  // bound of every device-side wait
 };
 
 struct CombineParams {

@@ -1,6 +1,7 @@
 // Launch entry points of the device kernels (host side of each .cu file).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ua_device.cuh"
@@ -40,6 +41,19 @@ bool prefill_supported(int head_dim, int kv_dtype, int qpk, int block_size);
 cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_cache,
                            const void* v_cache, int64_t total_q, int head_dim,
                            int num_kv_heads, cudaStream_t stream);
+
+// Tensor map of a row-major tensor (dims innermost first, strides in bytes of
+// dims 1..rank-1) for bf16 (elt_bytes 2) or byte (elt_bytes 1) elements.
+cudaError_t encode_tiled_map(CUtensorMap* map, int elt_bytes, int rank, const void* base,
+                             const uint64_t* dims, const uint64_t* strides_bytes,
+                             const uint32_t* box, bool swizzle_128b, bool l2_256b);
+
+// Tensor map over a paged cache [num_blocks][block_size][Hkv][head_dim] whose
+// box is (box_dims dims, one head, box_rows slots, one block); an out-of-range
+// block coordinate reads zeros.
+cudaError_t encode_kv_page_map(CUtensorMap* map, const void* cache, int elt_bytes, int head_dim,
+                               int num_kv_heads, int block_size, int64_t num_blocks,
+                               int box_dims, int box_rows, bool swizzle_128b);
 
 // Split-KV decode kernel over p.tiles[0 .. p.num_tiles).
 cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cudaStream_t stream);
