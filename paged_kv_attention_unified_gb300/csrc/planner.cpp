@@ -106,13 +106,11 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
     longest = std::max<int64_t>(longest, t.kv_hi - t.kv_lo);
   }
   int64_t chunk = 0;  // 0: do not split
-  if (p.num_splits == 0 && !dec.empty()) {
-    const int64_t target = static_cast<int64_t>(num_sms) * kDecodeCtasPerSm * kDecodeWaves;
-    if (static_cast<int64_t>(dec.size()) < target && total > 0) {
-      chunk = round_up(std::max<int64_t>(kMinSplitTokens, ceil_div(total, target)), kKeyStep);
-      chunk = std::max<int64_t>(chunk, round_up(ceil_div(longest, UA_MAX_SPLITS), kKeyStep));
-      if (chunk >= longest) chunk = 0;
-    }
+  if (p.num_splits == 0 && !dec.empty() && total > 0) {
+    const int64_t slots = static_cast<int64_t>(num_sms) * kDecodeCtasPerSm;
+    chunk = round_up(std::max<int64_t>(kMinSplitTokens, ceil_div(total, slots)), kKeyStep);
+    chunk = std::max<int64_t>(chunk, round_up(ceil_div(longest, UA_MAX_SPLITS), kKeyStep));
+    if (chunk >= longest) chunk = 0;
   }
   s.split_tokens = static_cast<int32_t>(chunk);
   int64_t slot = 0;

@@ -46,10 +46,10 @@ struct Schedule {
 // Granularity of key ranges: one decode step reads 16 tokens, so split pieces
 // and decode ranges start on multiples of 16.
 constexpr int kKeyStep = 16;
-// Decode kernel: resident CTAs per SM assumed when sizing automatic splits.
-constexpr int kDecodeCtasPerSm = 4;
-// Automatic splits aim for this many waves of decode CTAs.
-constexpr int kDecodeWaves = 2;
+// Decode kernel: resident CTAs per SM (three of 64 KB shared memory each),
+// used to size automatic splits: pieces of about the average load of one CTA
+// slot in a single wave, so that long sequences are cut and short ones not.
+constexpr int kDecodeCtasPerSm = 3;
 // Smallest automatic split piece, in key tokens.
 constexpr int kMinSplitTokens = 256;
 // Default: sequences with q_len * qpk above this go to the prefill kernel
