@@ -368,18 +368,25 @@ def run_ours(args):
     step_s = ms_max / 1e3 / args.steps
     value = _rate(cfg, byts * world, flops * world, step_s)
 
-    # dominant kernel and its roofline
+    # dominant kernel and its roofline, credited with the work of the sequences
+    # the scheduler gave it (host-only schedule of the same batch)
     kind = max(ktimes, key=lambda k: ktimes[k][0])
     kms, kn = ktimes[kind]
     avg_s = kms / 1e3 / max(kn, 1)
+    _, pre_t, dec_t, _ = ua.ua_schedule(b.cu_host, b.kv_host, b.num_q_heads, b.num_kv_heads,
+                                        b.head_dim, b.block_size, int(b.block_tables.shape[1]),
+                                        kv_dtype=b.kv_dtype, causal=b.causal, window=b.window,
+                                        num_sms=info.num_sms)
+    seqs = sorted({t["seq"] for t in (pre_t if kind == "prefill" else dec_t)})
+    k_bytes, k_flops = algorithmic_work(_seq_subcase(case, seqs)) if seqs else (byts, flops)
     if kind == "prefill":
-        ach = flops / avg_s / 1e12
+        ach = k_flops / avg_s / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
-                "frac": ach / tf_peak}
+                "frac": ach / tf_peak, "work_per_launch": k_flops}
     else:
-        ach = byts / avg_s / 1e9
+        ach = k_bytes / avg_s / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                "frac": ach / hbm_peak}
+                "frac": ach / hbm_peak, "work_per_launch": k_bytes}
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" \
         else "fallback"
     roof["kernel"] = kind

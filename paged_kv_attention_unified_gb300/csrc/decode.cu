@@ -156,10 +156,8 @@ __device__ __forceinline__ void compute_step(WarpState<D>& st, const StepRegs<D,
   for (int c = 0; c < C::NC; ++c) {
     uint32_t a[4];
     if constexpr (FP8) {
-      a[0] = e4m3x2_to_f16x2(r.k[0][c]);
-      a[1] = e4m3x2_to_f16x2(r.k[1][c]);
-      a[2] = e4m3x2_to_f16x2(r.k[0][c] >> 16);
-      a[3] = e4m3x2_to_f16x2(r.k[1][c] >> 16);
+      e4m3x4_to_f16x2x2(r.k[0][c], a[0], a[2]);
+      e4m3x4_to_f16x2x2(r.k[1][c], a[1], a[3]);
     } else {
       a[0] = r.k[0][2 * c];
       a[1] = r.k[1][2 * c];
@@ -223,10 +221,8 @@ __device__ __forceinline__ void compute_step(WarpState<D>& st, const StepRegs<D,
       const uint32_t sel = (c & 1) ? 0x7362u : 0x5140u;
       const uint32_t lo = __byte_perm(r.v[0][c >> 1], r.v[1][c >> 1], sel);
       const uint32_t hi = __byte_perm(r.v[2][c >> 1], r.v[3][c >> 1], sel);
-      a[0] = e4m3x2_to_f16x2(lo);
-      a[1] = e4m3x2_to_f16x2(lo >> 16);
-      a[2] = e4m3x2_to_f16x2(hi);
-      a[3] = e4m3x2_to_f16x2(hi >> 16);
+      e4m3x4_to_f16x2x2(lo, a[0], a[1]);
+      e4m3x4_to_f16x2x2(hi, a[2], a[3]);
     } else {
       a[0] = __byte_perm(r.v[0][c], r.v[1][c], 0x5410u);
       a[1] = __byte_perm(r.v[0][c], r.v[1][c], 0x7632u);

@@ -127,6 +127,19 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
 }
 
+// Four e4m3 codes in one word -> two f16x2 words (bytes 0,1 -> lo; bytes 2,3
+// -> hi; low byte -> low half). Two conversions, no repacking.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n"
+      ".reg .b16 l16, h16;\n"
+      "mov.b32 {l16, h16}, %2;\n"
+      "cvt.rn.f16x2.e4m3x2 %0, l16;\n"
+      "cvt.rn.f16x2.e4m3x2 %1, h16;\n"
+      "}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
+}
+
 __device__ __forceinline__ void record_error(int32_t* err, int32_t code) {
   if (err) atomicCAS(err, 0, code);
 }
