@@ -112,6 +112,9 @@ typedef struct {
   int64_t workspace_bytes;     /* bytes of split workspace the plan owns */
   int32_t split_tokens;        /* key tokens per split piece (0: no splits) */
   int32_t num_sms;             /* SM count the schedule was sized for */
+  int32_t num_prefill_ctas;    /* CTAs of the persistent prefill launch: min(num_sms, prefill
+                                  tiles); they take the prefill tiles in list order */
+  int32_t reserved;            /* zero */
 } ua_plan_info;
 
 typedef struct ua_plan ua_plan;

@@ -51,7 +51,8 @@ class ua_plan_info(ctypes.Structure):
     _fields_ = [("num_prefill_tiles", ctypes.c_int64), ("num_decode_tiles", ctypes.c_int64),
                 ("num_combine_groups", ctypes.c_int64), ("num_slots", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("split_tokens", ctypes.c_int32),
-                ("num_sms", ctypes.c_int32)]
+                ("num_sms", ctypes.c_int32), ("num_prefill_ctas", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class UAError(RuntimeError):

@@ -180,6 +180,50 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
                        return longer(a, b);
                      });
   }
+  // 4. The persistent prefill CTAs take tiles in list order as they free up.
+  // The bulk keeps the order above; the shortest tiles, up to
+  // kPrefillTailShare of the work, move to the end, longest first, so that no
+  // CTA starts a long tile while the others run dry.
+  if (!s.prefill.empty()) {
+    const size_t n = s.prefill.size();
+    std::vector<int64_t> cost(n, 0);
+    int64_t total_cost = 0;
+    for (size_t i = 0; i < n; ++i) {
+      const ua_tile& t = s.prefill[i];
+      const int32_t ql = p.cu_query_lens[t.seq + 1] - p.cu_query_lens[t.seq];
+      for (int32_t r0 = t.row0; r0 < t.row0 + t.nrows; r0 += kPrefillQueryTile) {
+        int32_t lo = 0, hi = 0;
+        const int32_t rows = std::min(kPrefillQueryTile, t.row0 + t.nrows - r0);
+        key_range(p, p.kv_lens[t.seq] - ql, p.kv_lens[t.seq], r0, rows, &lo, &hi);
+        cost[i] += ceil_div(std::max<int64_t>(0, hi - t.kv_lo), kPrefillKeyTile);
+      }
+      total_cost += cost[i];
+    }
+    std::vector<size_t> by_cost(n);
+    for (size_t i = 0; i < n; ++i) by_cost[i] = i;
+    std::stable_sort(by_cost.begin(), by_cost.end(),
+                     [&](size_t a, size_t b) { return cost[a] < cost[b]; });
+    std::vector<char> in_tail(n, 0);
+    int64_t tail_cost = 0;
+    for (size_t k = 0; k < n; ++k) {
+      const size_t i = by_cost[k];
+      if (static_cast<double>(tail_cost + cost[i]) > kPrefillTailShare * total_cost) break;
+      tail_cost += cost[i];
+      in_tail[i] = 1;
+    }
+    std::vector<ua_tile> bulk, tail;
+    std::vector<int64_t> tail_c;
+    for (size_t i = 0; i < n; ++i) (in_tail[i] ? tail : bulk).push_back(s.prefill[i]);
+    for (size_t i = 0; i < n; ++i)
+      if (in_tail[i]) tail_c.push_back(cost[i]);
+    std::vector<size_t> tail_order(tail.size());
+    for (size_t k = 0; k < tail.size(); ++k) tail_order[k] = k;
+    std::stable_sort(tail_order.begin(), tail_order.end(),
+                     [&](size_t a, size_t b) { return tail_c[a] > tail_c[b]; });
+    s.prefill = std::move(bulk);
+    for (size_t k : tail_order) s.prefill.push_back(tail[k]);
+    s.prefill_ctas = static_cast<int32_t>(std::min<int64_t>(num_sms, static_cast<int64_t>(n)));
+  }
   *out = std::move(s);
   return UA_OK;
 }

@@ -34,7 +34,9 @@ struct Problem {
 };
 
 struct Schedule {
+  // Prefill tiles in the order the persistent prefill CTAs take them.
   std::vector<ua_tile> prefill;
+  int32_t prefill_ctas = 0;  // persistent prefill CTAs: min(SMs, prefill tiles)
   std::vector<ua_tile> decode;
   std::vector<ua_combine_group> groups;
   int64_t num_slots = 0;
@@ -57,6 +59,11 @@ constexpr int kMinSplitTokens = 256;
 constexpr int kDefaultDecodeRowsMax = 32;
 // Key tile of the prefill kernel: its key ranges start on multiples of this.
 constexpr int kPrefillKeyTile = 128;
+// Rows of one tcgen05 query tile of the prefill kernel (two per prefill tile).
+constexpr int kPrefillQueryTile = 128;
+// Share of the prefill work (in 128 x 128 query-key blocks) kept for the end
+// of the prefill list: the shortest tiles, so that the CTAs finish together.
+constexpr double kPrefillTailShare = 1.0 / 16.0;
 
 // Validate the problem (host arrays included).
 ua_status validate(const Problem& p);

@@ -1,5 +1,5 @@
-// Prefill kernel (K-P): tcgen05 / TMEM / TMA attention, two 128-row query
-// tiles per CTA.
+// Prefill kernel (K-P): tcgen05 / TMEM / TMA attention, persistent, two
+// 128-row query tiles per work tile.
 //
 // Work unit: one ua_tile of up to 256 packed rows (tokens x the qpk query
 // heads of one KV head, the packed GQA tile of
@@ -9,15 +9,21 @@
 // (S = Q K^T, online softmax in base 2, O += P V, O / l at the end); the two
 // query tiles are interleaved on the tensor core in the ping-pong manner the
 // notes describe for FlashAttention-3, so that one tile's softmax overlaps
-// the other tile's matrix products:
-//   warp 0      TMA producer of Q (both tiles) and of the K ring, and
+// the other tile's matrix products.
+// One CTA per SM (at most) takes work tiles from a queue in list order as it
+// frees up; the rings and barrier phases run on from one work tile to the
+// next, so the next tile's Q and first K/V tiles load while the current one
+// finishes, and its output store overlaps the next tile's first products.
+//   warp 0      TMA producer of Q (per query tile, refilled once the last S
+//               MMA of the previous work tile has read it) and of the K ring;
 //   warp 2      TMA producer of the V ring (one box per page, resolved through
 //               the block table);
 //   warp 1      owns the tensor memory; one thread issues the MMAs in the order
 //               S0(j) S1(j) | PV0(j) S0(j+1) | PV1(j) S1(j+1) | ...
 //               (S_t into TMEM columns 128t, O_t into 256 + 128t; P_t is read
 //               from TMEM where the softmax wrote it over S_t);
-//   warp 3      idle (it completes the control warpgroup);
+//   warp 3      scheduler: one thread claims the next work tile and hands it
+//               to the other roles through a shared-memory descriptor;
 //   warps 4-7   softmax of query tile 0, one row per thread (TMEM lane);
 //   warps 8-11  softmax of query tile 1.
 // Softmax: scale, mask by select, running max / sum, P = 2^(x - m) stored as
@@ -50,6 +56,14 @@ constexpr uint32_t kSoftmaxRegs = 224;
 constexpr int kLaunchRegs = 168;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// Work-tile descriptors the scheduler warp keeps ahead: one. A CTA claims its
+// next tile only when every role has started the current one, which keeps
+// the claims close to the order in which the CTAs run dry.
+constexpr int kItemSlots = 1;
+constexpr int kItemBytes = 64;  // one descriptor in shared memory
+// Arrivals that free a descriptor slot: the two producer threads, the MMA
+// thread and the eight softmax warps (one lane each).
+constexpr int kItemConsumers = 3 + 8;
 
 template <int D>
 struct Smem {
@@ -61,41 +75,56 @@ struct Smem {
   static constexpr int kK = kQ + kTilesPerCta * kTile;
   static constexpr int kV = kK + kKStages * kTile;
   static constexpr int kBar = kV + kVStages * kTile;
-  // q_full, kfull/kempty[KS], vfull/vempty[VS], s_full/p_ready/o_done[2], mma_done
-  static constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 3 * kTilesPerCta + 1;
+  // q_full/q_empty[2], kfull/kempty[KS], vfull/vempty[VS], s_full/p_ready/o_done[2],
+  // mma_done, item_full/item_empty[kItemSlots]
+  static constexpr int kNumBars = 2 * kTilesPerCta + 2 * kKStages + 2 * kVStages +
+                                  3 * kTilesPerCta + 1 + 2 * kItemSlots;
   static constexpr int kMisc = kBar + 8 * kNumBars;
-  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kItems = kMisc + 64;
+  static constexpr int kBytes = kItems + kItemSlots * kItemBytes;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
 
+// The CTA's mbarriers as 32-bit shared-window addresses: one base register
+// and constant offsets (8 bytes per barrier).
+template <int D>
 struct Bars {
-  uint64_t* q_full;
-  uint64_t* kfull;
-  uint64_t* kempty;
-  uint64_t* vfull;
-  uint64_t* vempty;
-  uint64_t* s_full;   // [2]
-  uint64_t* p_ready;  // [2]
-  uint64_t* o_done;   // [2]
-  uint64_t* mma_done;
+  static constexpr int KS = Smem<D>::kKStages, VS = Smem<D>::kVStages;
+  uint32_t base;
+  __device__ __forceinline__ uint32_t at(int i) const { return base + 8u * static_cast<uint32_t>(i); }
+  __device__ __forceinline__ uint32_t q_full(int t) const { return at(t); }   // Q of query tile t landed
+  __device__ __forceinline__ uint32_t q_empty(int t) const {                  // its last S MMA read it
+    return at(kTilesPerCta + t);
+  }
+  __device__ __forceinline__ uint32_t kfull(int s) const { return at(2 * kTilesPerCta + s); }
+  __device__ __forceinline__ uint32_t kempty(int s) const { return at(2 * kTilesPerCta + KS + s); }
+  __device__ __forceinline__ uint32_t vfull(int s) const {
+    return at(2 * kTilesPerCta + 2 * KS + s);
+  }
+  __device__ __forceinline__ uint32_t vempty(int s) const {
+    return at(2 * kTilesPerCta + 2 * KS + VS + s);
+  }
+  __device__ __forceinline__ uint32_t s_full(int t) const {
+    return at(2 * kTilesPerCta + 2 * KS + 2 * VS + t);
+  }
+  __device__ __forceinline__ uint32_t p_ready(int t) const {
+    return at(3 * kTilesPerCta + 2 * KS + 2 * VS + t);
+  }
+  __device__ __forceinline__ uint32_t o_done(int t) const {
+    return at(4 * kTilesPerCta + 2 * KS + 2 * VS + t);
+  }
+  __device__ __forceinline__ uint32_t mma_done() const {
+    return at(5 * kTilesPerCta + 2 * KS + 2 * VS);
+  }
+  __device__ __forceinline__ uint32_t item_full(int s) const {   // descriptor s written
+    return at(5 * kTilesPerCta + 2 * KS + 2 * VS + 1 + s);
+  }
+  __device__ __forceinline__ uint32_t item_empty(int s) const {  // every role has read it
+    return at(5 * kTilesPerCta + 2 * KS + 2 * VS + 1 + kItemSlots + s);
+  }
 };
 
-template <int KS, int VS>
-__device__ __forceinline__ Bars bars_at(uint64_t* b) {
-  Bars r;
-  r.q_full = b;
-  r.kfull = b + 1;
-  r.kempty = r.kfull + KS;
-  r.vfull = r.kempty + KS;
-  r.vempty = r.vfull + VS;
-  r.s_full = r.vempty + VS;
-  r.p_ready = r.s_full + kTilesPerCta;
-  r.o_done = r.p_ready + kTilesPerCta;
-  r.mma_done = r.o_done + kTilesPerCta;
-  return r;
-}
-
-// Per-CTA geometry shared by every role.
+// Geometry of one work tile, computed the same way by every role.
 struct Geometry {
   int q_start, ctx, nrows, kv_lo, kv_hi;
   int rows[kTilesPerCta];    // valid rows of each query tile
@@ -103,193 +132,367 @@ struct Geometry {
   int nmax;                  // key tiles loaded
 };
 
+// One work tile as the scheduler warp hands it to the other roles.
+struct Item {
+  int seq, kv_head, row0;
+  int end;  // 1: no more work tiles for this CTA
+  Geometry g;
+};
+static_assert(sizeof(Item) <= kItemBytes, "work-tile descriptor too large");
+
+// Per-sequence values from the device arrays; ranges are clamped so that
+// disagreeing host/device lengths cannot send a read out of bounds.
+__device__ __forceinline__ Geometry geometry_of(const PrefillParams& p, const ua_tile& tile) {
+  Geometry g;
+  g.q_start = p.cu_query_lens[tile.seq];
+  const int qlen = p.cu_query_lens[tile.seq + 1] - g.q_start;
+  const int kv_len = p.kv_lens[tile.seq];
+  g.ctx = kv_len - qlen;
+  g.nrows = min(tile.nrows, qlen * p.qpk - tile.row0);
+  g.kv_hi = min(min(tile.kv_hi, kv_len), p.max_blocks_per_seq * p.block_size);
+  g.kv_lo = tile.kv_lo;
+  g.nmax = 0;
+#pragma unroll
+  for (int t = 0; t < kTilesPerCta; ++t) {
+    g.rows[t] = max(0, min(kRows, g.nrows - t * kRows));
+    g.ntiles[t] = 0;
+    if (g.rows[t] > 0) {
+      const int last = tile.row0 + t * kRows + g.rows[t] - 1;
+      const int hi = p.causal ? min(g.kv_hi, g.ctx + last / p.qpk + 1) : g.kv_hi;
+      g.ntiles[t] = hi > g.kv_lo ? (hi - g.kv_lo + kKeys - 1) / kKeys : 0;
+    }
+    g.nmax = max(g.nmax, g.ntiles[t]);
+  }
+  return g;
+}
+
 // Give up: record the error once and tell the other roles.
 __device__ __forceinline__ void give_up(const PrefillParams& p, volatile int32_t* abort) {
   record_error(p.err, UA_ERR_DEVICE_TIMEOUT);
   *abort = 1;
 }
 
-// ------------------------------------------------------------------ producer
-// One thread of warp 0: Q of both query tiles, then the K ring. One thread of
-// warp 2: the V ring.
-// Every page id is read from the block table and checked; a missing or
-// out-of-range page is loaded from an out-of-range block coordinate, which
-// TMA fills with zeros.
-template <int D, bool kIsV>
-__device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CUtensorMap* map_kv,
-                                              const PrefillParams& p, const ua_tile& tile,
-                                              const Geometry& g, uint8_t* sQ, uint8_t* sRing,
-                                              uint64_t* full, uint64_t* empty, int stages,
-                                              uint64_t* q_full, volatile int32_t* abort,
-                                              volatile int32_t* never) {
+// ------------------------------------------------------------------ scheduler
+// One thread of warp 3 claims the CTA's next work tile from the shared queue
+// (p.counters[0], a ticket per claim), reads it and the sequence lengths it
+// needs from global memory, and publishes it in a shared-memory ring; the
+// other roles never wait on a global load between work tiles (those loads
+// would queue behind the previous tile's output stores). When the queue is
+// empty it publishes an end marker. The last CTA to finish (p.counters[1])
+// resets both counters for the next launch; a CTA that gives up still counts
+// itself, so the reset happens on the error path too.
+template <int D>
+__device__ __forceinline__ void scheduler_role(const PrefillParams& p, const Bars<D>& bar,
+                                               uint8_t* ring, volatile int32_t* abort) {
+  for (int k = 0;; ++k) {
+    const int s = k % kItemSlots;
+    if (k >= kItemSlots &&
+        !mbar_wait(bar.item_empty(s), ((k / kItemSlots) - 1) & 1, abort, p.timeout_ns)) {
+      give_up(p, abort);
+      break;
+    }
+    Item it = {};
+    const int idx = atomicAdd(&p.counters[0], 1);
+    it.end = idx >= p.num_tiles ? 1 : 0;
+    if (!it.end) {
+      const ua_tile tile = p.tiles[idx];
+      it.seq = tile.seq;
+      it.kv_head = tile.kv_head;
+      it.row0 = tile.row0;
+      it.g = geometry_of(p, tile);
+    }
+    *reinterpret_cast<Item*>(ring + s * kItemBytes) = it;
+    mbar_arrive(bar.item_full(s));  // release: the descriptor is visible to its readers
+    if (it.end) break;
+  }
+  __threadfence();
+  if (atomicAdd(&p.counters[1], 1) == static_cast<int>(gridDim.x) - 1) {
+    atomicExch(&p.counters[0], 0);
+    atomicExch(&p.counters[1], 0);
+  }
+}
+
+// Wait for work-tile descriptor k and copy it out of the ring. The caller
+// then frees the slot (one arrival per consumer thread or softmax warp).
+template <int D>
+__device__ __forceinline__ bool take_item(const PrefillParams& p, const Bars<D>& bar,
+                                          const uint8_t* ring, int k, Item& it,
+                                          volatile int32_t* abort) {
+  const int s = k % kItemSlots;
+  if (!mbar_wait(bar.item_full(s), (k / kItemSlots) & 1, abort, p.timeout_ns)) return false;
+  it = *reinterpret_cast<const Item*>(ring + s * kItemBytes);
+  return true;
+}
+
+// ------------------------------------------------------------------ producers
+// Key tile j of a work tile into one ring slot: one TMA box per page (or per
+// 128 rows of a larger page) and 64-wide panel. Every page id is read from
+// the block table and checked; a missing or out-of-range page is loaded from
+// an out-of-range block coordinate, which TMA fills with zeros.
+template <int D>
+__device__ __forceinline__ void load_key_tile(const CUtensorMap* map, const PrefillParams& p,
+                                              const Item& tile, const Geometry& g, int j,
+                                              uint8_t* dst, uint32_t full) {
   using L = Smem<D>;
   constexpr int kPanels = D / 64;
-  prefetch_tmap(map_kv);
-  const bool idle = (p.debug_flags & kDebugProducerIdle) != 0;
-  int last_phase[4] = {-1, -1, -1, -1};
-  if (!idle) {
-    if (!kIsV) {
-      prefetch_tmap(map_q);
-      int active = 0;
-      for (int t = 0; t < kTilesPerCta; ++t) active += g.rows[t] > 0;
-      mbar_arrive_expect_tx(q_full, active * kRows * D * 2);
-      for (int t = 0; t < kTilesPerCta; ++t) {
-        if (g.rows[t] <= 0) continue;
-        for (int pn = 0; pn < kPanels; ++pn)
-          tma_load_3d(sQ + t * L::kTile + pn * L::kPanel, map_q, q_full, pn * 64,
-                      tile.kv_head * p.qpk, g.q_start + (tile.row0 + t * kRows) / p.qpk);
+  const int boxes = kKeys / p.rows_per_box;
+  const int base = g.kv_lo + j * kKeys;
+  mbar_arrive_expect_tx(full, kKeys * D * 2);
+  for (int b = 0; b < boxes; ++b) {
+    const int key0 = base + b * p.rows_per_box;
+    int32_t blk = static_cast<int32_t>(p.num_blocks);  // out of range: zero fill
+    int32_t slot = 0;
+    if (key0 < g.kv_hi) {
+      const int32_t id =
+          p.block_tables[static_cast<int64_t>(tile.seq) * p.max_blocks_per_seq + key0 / p.block_size];
+      if (id >= 0 && static_cast<int64_t>(id) < p.num_blocks) {
+        blk = id;
+        slot = key0 % p.block_size;
+      } else {
+        record_error(p.err, UA_ERR_BOUNDS);
       }
     }
-    const int boxes = kKeys / p.rows_per_box;
-    for (int j = 0; j < g.nmax; ++j) {
-      const int s = j % stages;
-      if (j >= stages &&
-          !mbar_wait(&empty[s], ((j / stages) - 1) & 1, abort, p.timeout_ns)) {
-        give_up(p, abort);
+    const int row_off = b * p.rows_per_box * 128;
+#pragma unroll
+    for (int pn = 0; pn < kPanels; ++pn)
+      tma_load_4d(dst + pn * L::kPanel + row_off, map, full, pn * 64, tile.kv_head, slot, blk);
+  }
+}
+
+// One thread of warp 0: per work tile, Q of query tile 0, the K ring, and Q
+// of query tile 1 after the first key tile (a Q buffer is refilled once the
+// last S MMA of the previous work tile has read it). One thread of warp 2
+// (kIsV): the V ring. Ring positions run on across the CTA's work tiles.
+template <int D, bool kIsV>
+__device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CUtensorMap* map_kv,
+                                              const PrefillParams& p, const uint8_t* ring,
+                                              uint8_t* sQ, uint8_t* sRing, uint32_t full,
+                                              uint32_t empty, const Bars<D>& bar,
+                                              volatile int32_t* abort, volatile int32_t* never) {
+  using L = Smem<D>;
+  constexpr int kPanels = D / 64;
+  constexpr int kStages = kIsV ? L::kVStages : L::kKStages;
+  prefetch_tmap(map_kv);
+  if (!kIsV) prefetch_tmap(map_q);
+  const bool idle = (p.debug_flags & kDebugProducerIdle) != 0;
+  int last_phase[kStages];
+#pragma unroll
+  for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
+  int q_loads[kTilesPerCta] = {0, 0};
+  bool ok = true;
+  // Q of query tile t is loaded exactly when the MMA issuer will consume it.
+  auto load_q = [&](const Item& tile, const Geometry& g, int t) {
+    if (g.ntiles[t] <= 0) return true;
+    if (q_loads[t] > 0 &&
+        !mbar_wait(bar.q_empty(t), (q_loads[t] - 1) & 1, abort, p.timeout_ns))
+      return false;
+    mbar_arrive_expect_tx(bar.q_full(t), kRows * D * 2);
+#pragma unroll
+    for (int pn = 0; pn < kPanels; ++pn)
+      tma_load_3d(sQ + t * L::kTile + pn * L::kPanel, map_q, bar.q_full(t), pn * 64,
+                  tile.kv_head * p.qpk, g.q_start + (tile.row0 + t * kRows) / p.qpk);
+    ++q_loads[t];
+    return true;
+  };
+  if (!idle) {
+    int step = 0;  // position in the ring sequence
+    for (int k = 0; ok; ++k) {
+      Item tile;
+      if (!take_item<D>(p, bar, ring, k, tile, abort)) {
+        ok = false;
         break;
       }
-      const int base = g.kv_lo + j * kKeys;
-      mbar_arrive_expect_tx(&full[s], kKeys * D * 2);
-      for (int b = 0; b < boxes; ++b) {
-        const int key0 = base + b * p.rows_per_box;
-        int32_t blk = static_cast<int32_t>(p.num_blocks);  // out of range: zero fill
-        int32_t slot = 0;
-        if (key0 < g.kv_hi) {
-          const int32_t id = p.block_tables[static_cast<int64_t>(tile.seq) *
-                                                p.max_blocks_per_seq + key0 / p.block_size];
-          if (id >= 0 && static_cast<int64_t>(id) < p.num_blocks) {
-            blk = id;
-            slot = key0 % p.block_size;
-          } else {
-            record_error(p.err, UA_ERR_BOUNDS);
-          }
+      mbar_arrive(bar.item_empty(k % kItemSlots));
+      if (tile.end) break;
+      const Geometry& g = tile.g;
+      if (g.nmax <= 0) continue;
+      if (!kIsV) ok = load_q(tile, g, 0);
+      for (int j = 0; ok && j < g.nmax; ++j, ++step) {
+        const int s = step % kStages;
+        if (step >= kStages &&
+            !mbar_wait(empty + 8u * s, ((step / kStages) - 1) & 1, abort, p.timeout_ns)) {
+          ok = false;
+          break;
         }
-        const int row_off = b * p.rows_per_box * 128;
-        for (int pn = 0; pn < kPanels; ++pn)
-          tma_load_4d(sRing + s * L::kTile + pn * L::kPanel + row_off, map_kv, &full[s],
-                      pn * 64, tile.kv_head, slot, blk);
+        load_key_tile<D>(map_kv, p, tile, g, j, sRing + s * L::kTile, full + 8u * s);
+        last_phase[s] = step / kStages;
+        if (!kIsV && j == 0) ok = load_q(tile, g, 1);
       }
-      last_phase[s] = j / stages;
     }
+    if (!ok) give_up(p, abort);
   }
   // Drain: every load issued completes before the CTA may exit.
-  for (int s = 0; s < stages; ++s)
-    if (last_phase[s] >= 0 && !mbar_wait(&full[s], last_phase[s] & 1, never, p.timeout_ns))
+#pragma unroll
+  for (int s = 0; s < kStages; ++s)
+    if (last_phase[s] >= 0 && !mbar_wait(full + 8u * s, last_phase[s] & 1, never, p.timeout_ns))
       give_up(p, abort);
-  if (!kIsV && !idle && !mbar_wait(q_full, 0, never, p.timeout_ns)) give_up(p, abort);
+  if (!kIsV) {
+#pragma unroll
+    for (int t = 0; t < kTilesPerCta; ++t)
+      if (q_loads[t] > 0 && !mbar_wait(bar.q_full(t), (q_loads[t] - 1) & 1, never, p.timeout_ns))
+        give_up(p, abort);
+  }
 }
 
 // ------------------------------------------------------------------ MMA issuer
+// Per work tile: S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...; ring
+// positions and the per-query-tile barrier phases run on across work tiles.
 template <int D>
-__device__ __forceinline__ void mma_role(const PrefillParams& p, const Geometry& g, uint8_t* sQ,
+__device__ __forceinline__ void mma_role(const PrefillParams& p, const uint8_t* ring, uint8_t* sQ,
                                          uint8_t* sK, uint8_t* sV, uint32_t tmem,
-                                         const Bars& bar, volatile int32_t* abort,
+                                         const Bars<D>& bar, volatile int32_t* abort,
                                          volatile int32_t* never) {
   using L = Smem<D>;
   constexpr int KS = L::kKStages, VS = L::kVStages;
   constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);
   constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 0, 1);
-  auto issue_s = [&](int t, int j) {
-    const uint32_t q_addr = smem_u32(sQ + t * L::kTile);
-    const uint32_t k_addr = smem_u32(sK + (j % KS) * L::kTile);
+  // Each operand descriptor is built once per group of MMAs; the k-th MMA
+  // adds its byte offset / 16 to the 14-bit start-address field (shared
+  // addresses stay below 256 KB, so the field cannot overflow).
+  auto issue_s = [&](int t, int gj) {
+    const uint64_t qd = smem_desc_sw128(opaque_u32(smem_u32(sQ)) + t * L::kTile, 16, 1024);
+    const uint64_t kd = smem_desc_sw128(smem_u32(sK) + (gj % KS) * L::kTile, 16, 1024);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k) {
-      const uint32_t off = (k / 4) * L::kPanel + (k % 4) * 32;
-      mma_ss(tmem + t * kKeys, smem_desc_sw128(q_addr + off, 16, 1024),
-             smem_desc_sw128(k_addr + off, 16, 1024), idesc_s, k > 0 ? 1u : 0u);
+      const uint64_t off = static_cast<uint64_t>(((k / 4) * L::kPanel + (k % 4) * 32) >> 4);
+      mma_ss(tmem + t * kKeys, qd + off, kd + off, idesc_s, k > 0 ? 1u : 0u);
     }
-    mma_commit(&bar.s_full[t]);
+    mma_commit(bar.s_full(t));
   };
-  auto issue_pv = [&](int t, int j) {
-    const uint32_t v_addr = smem_u32(sV + (j % VS) * L::kTile);
+  auto issue_pv = [&](int t, int gj, bool acc) {
+    const uint64_t vd = smem_desc_sw128(smem_u32(sV) + (gj % VS) * L::kTile, L::kPanel, 1024);
 #pragma unroll
     for (int k = 0; k < kKeys / 16; ++k)
       mma_ts(tmem + 256 + t * 128, tmem + t * kKeys + 8 * k,
-             smem_desc_sw128(v_addr + k * 2048, L::kPanel, 1024), idesc_o,
-             (j > 0 || k > 0) ? 1u : 0u);
-    mma_commit(&bar.o_done[t]);
+             vd + static_cast<uint64_t>((k * 2048) >> 4), idesc_o, (acc || k > 0) ? 1u : 0u);
+    mma_commit(bar.o_done(t));
   };
-  const int n0 = g.ntiles[0], n1 = g.ntiles[1];
-  bool ok = mbar_wait(bar.q_full, 0, abort, p.timeout_ns) &&
-            mbar_wait(&bar.kfull[0], 0, abort, p.timeout_ns);
-  if (ok) {
-    tc_fence_after();
-    if (n0 > 0) issue_s(0, 0);
-    if (n1 > 0) issue_s(1, 0);
-    mma_commit(&bar.kempty[0]);
-  }
-  for (int j = 0; ok && j < g.nmax; ++j) {
-    if (!mbar_wait(&bar.vfull[j % VS], (j / VS) & 1, abort, p.timeout_ns)) {
+  int step = 0;                       // ring position of key tile 0 of the work tile
+  int done[kTilesPerCta] = {0, 0};    // key tiles of each query tile so far
+  int q_used[kTilesPerCta] = {0, 0};  // Q loads consumed per query tile
+  bool ok = true;
+  for (int k = 0; ok; ++k) {
+    Item it;
+    if (!take_item<D>(p, bar, ring, k, it, abort)) {
       ok = false;
       break;
     }
-    if (j < n0) {
-      if (!mbar_wait(&bar.p_ready[0], j & 1, abort, p.timeout_ns)) {
+    mbar_arrive(bar.item_empty(k % kItemSlots));
+    if (it.end) break;
+    const Geometry& g = it.g;
+    if (g.nmax <= 0) continue;
+    const int n0 = g.ntiles[0], n1 = g.ntiles[1];
+    ok = mbar_wait(bar.kfull(step % KS), (step / KS) & 1, abort, p.timeout_ns);
+    if (ok && n0 > 0) {
+      ok = mbar_wait(bar.q_full(0), q_used[0] & 1, abort, p.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, step);
+        if (n0 == 1) mma_commit(bar.q_empty(0));
+      }
+    }
+    if (ok && n1 > 0) {
+      ok = mbar_wait(bar.q_full(1), q_used[1] & 1, abort, p.timeout_ns);
+      if (ok) {
+        tc_fence_after();
+        issue_s(1, step);
+        if (n1 == 1) mma_commit(bar.q_empty(1));
+      }
+    }
+    if (!ok) break;
+    mma_commit(bar.kempty(step % KS));
+    for (int j = 0; j < g.nmax; ++j) {
+      const int gj = step + j;
+      if (!mbar_wait(bar.vfull(gj % VS), (gj / VS) & 1, abort, p.timeout_ns)) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      issue_pv(0, j);
-    }
-    const bool more = j + 1 < g.nmax;
-    if (more) {
-      if (!mbar_wait(&bar.kfull[(j + 1) % KS], ((j + 1) / KS) & 1, abort, p.timeout_ns)) {
-        ok = false;
-        break;
+      if (j < n0) {
+        if (!mbar_wait(bar.p_ready(0), (done[0] + j) & 1, abort, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(0, gj, j > 0);
       }
-      tc_fence_after();
-      if (j + 1 < n0) issue_s(0, j + 1);
-    }
-    if (j < n1) {
-      if (!mbar_wait(&bar.p_ready[1], j & 1, abort, p.timeout_ns)) {
-        ok = false;
-        break;
+      const bool more = j + 1 < g.nmax;
+      if (more) {
+        if (!mbar_wait(bar.kfull((gj + 1) % KS), ((gj + 1) / KS) & 1, abort, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (j + 1 < n0) {
+          issue_s(0, gj + 1);
+          if (j + 2 == n0) mma_commit(bar.q_empty(0));
+        }
       }
-      tc_fence_after();
-      issue_pv(1, j);
+      if (j < n1) {
+        if (!mbar_wait(bar.p_ready(1), (done[1] + j) & 1, abort, p.timeout_ns)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(1, gj, j > 0);
+      }
+      mma_commit(bar.vempty(gj % VS));
+      if (more) {
+        if (j + 1 < n1) {
+          issue_s(1, gj + 1);
+          if (j + 2 == n1) mma_commit(bar.q_empty(1));
+        }
+        mma_commit(bar.kempty((gj + 1) % KS));
+      }
     }
-    mma_commit(&bar.vempty[j % VS]);
-    if (more) {
-      if (j + 1 < n1) issue_s(1, j + 1);
-      mma_commit(&bar.kempty[(j + 1) % KS]);
-    }
+    step += g.nmax;
+    done[0] += n0;
+    done[1] += n1;
+    q_used[0] += n0 > 0;
+    q_used[1] += n1 > 0;
   }
   if (!ok) give_up(p, abort);
   // Drain: every MMA issued has completed before the tensor memory is freed.
-  mma_commit(bar.mma_done);
-  if (!mbar_wait(bar.mma_done, 0, never, p.timeout_ns)) give_up(p, abort);
+  mma_commit(bar.mma_done());
+  if (!mbar_wait(bar.mma_done(), 0, never, p.timeout_ns)) give_up(p, abort);
 }
-
 // ------------------------------------------------------------------ softmax
-// Query tile t, one thread per row r (TMEM lane r). A warp may only touch TMEM
-// lanes 32 * (warp % 4) .. + 31, which fixes the rows of each warp.
+// What the softmax of one query tile needs of a work tile, as scalars (a
+// runtime index into the descriptor would put it in local memory).
+struct SoftmaxTile {
+  int kv_head, row0, q_start, ctx, kv_lo, kv_hi, nmax;
+  int n_t;     // key tiles of this query tile
+  int rows_t;  // valid rows of this query tile
+};
+
+// Query tile t of one work tile, one thread per row r (TMEM lane r). A warp may
+// only touch TMEM lanes 32 * (warp % 4) .. + 31, which fixes the rows of each
+// warp. `done` is the number of key tiles this query tile has already had in
+// earlier work tiles (barrier phases), `step` the ring position of key tile 0.
 template <int D>
-__device__ __forceinline__ void softmax_role(const PrefillParams& p, const ua_tile& tile,
-                                             const Geometry& g, int t, uint8_t* sV,
-                                             uint32_t tmem, const Bars& bar,
-                                             volatile int32_t* abort, int warp, int lane) {
+__device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const SoftmaxTile& g, int t,
+                                             int done, int step, uint8_t* sV, uint32_t tmem,
+                                             const Bars<D>& bar, volatile int32_t* abort,
+                                             int warp, int lane) {
   using L = Smem<D>;
   constexpr int kPanels = D / 64;
   constexpr int VS = L::kVStages;
-  const int n_t = g.ntiles[t];
-  if (n_t <= 0) return;
+  const int n_t = g.n_t;
   const uint32_t quarter = static_cast<uint32_t>(warp & 3);
   const int r = static_cast<int>(quarter) * 32 + lane;
   const uint32_t lane_addr = (quarter * 32) << 16;
   const uint32_t s_tmem = tmem + lane_addr + t * kKeys;
   const uint32_t o_tmem = tmem + lane_addr + 256 + t * 128;
-  const int rr = min(r, g.rows[t] - 1);   // rows past the end behave like the last one
-  const int row = tile.row0 + t * kRows + rr;
+  const int rr = min(r, g.rows_t - 1);   // rows past the end behave like the last one
+  const int row = g.row0 + t * kRows + rr;
   const int pos = g.ctx + row / p.qpk;
   // Scores are used as x = s * c with c >= 0: a negative scale flips the sign
   // of the raw scores once, so that the row max is always a max.
   const bool neg = p.score_scale_log2 < 0.f;
   const float c = neg ? -p.score_scale_log2 : p.score_scale_log2;
   float m = -INFINITY, l = 0.f;
-  bool ok = true;
   for (int j = 0; j < n_t; ++j) {
-    ok = __all_sync(0xffffffffu, mbar_wait(&bar.s_full[t], j & 1, abort, p.timeout_ns));
-    if (!ok) break;
+    if (!__all_sync(0xffffffffu, mbar_wait(bar.s_full(t), (done + j) & 1, abort, p.timeout_ns)))
+      return false;
     tc_fence_after();
     const int base = g.kv_lo + j * kKeys;
     // Raw scores; the scale is folded into one fma per pair below.
@@ -349,13 +552,15 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const ua_ti
     sum2[0] = f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3]));
     float sum_lo, sum_hi;
     f2_unpack(sum2[0], sum_lo, sum_hi);
-    const float rowsum = sum_lo + sum_hi;
-    l = l * alpha + rowsum;
+    l = l * alpha + (sum_lo + sum_hi);
     m = m_use;
-    // Rescale O in TMEM when some row of this warp moved its max.
+    // Rescale O in TMEM when some row of this warp moved its max (after the
+    // exponentials: the raw scores are dead by then, which keeps the register
+    // peak low).
     if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_done[t], (j - 1) & 1, abort, p.timeout_ns));
-      if (!ok) break;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(bar.o_done(t), (done + j - 1) & 1, abort, p.timeout_ns)))
+        return false;
       tc_fence_after();
 #pragma unroll
       for (int ch = 0; ch < D / 32; ++ch) {
@@ -380,9 +585,10 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const ua_ti
     // (they can hold anything, and 0 * NaN would reach O).
     const int valid = g.kv_hi - base;
     if (valid < kKeys && j == g.nmax - 1) {
-      const int sv = j % VS;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar.vfull[sv], (j / VS) & 1, abort, p.timeout_ns));
-      if (!ok) break;
+      const int gj = step + j;
+      const int sv = gj % VS;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar.vfull(sv), (gj / VS) & 1, abort, p.timeout_ns)))
+        return false;
       uint8_t* vt = sV + sv * L::kTile;
       const int dead = kKeys - valid;
       for (int idx = r; idx < dead * kPanels * 8; idx += kRows) {
@@ -393,20 +599,18 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const ua_ti
       fence_proxy_async_smem();
     }
     tc_fence_before();
-    mbar_arrive(&bar.p_ready[t]);
+    mbar_arrive(bar.p_ready(t));
   }
-  if (ok)
-    ok = __all_sync(0xffffffffu, mbar_wait(&bar.o_done[t], (n_t - 1) & 1, abort, p.timeout_ns));
-  if (!ok) {
-    give_up(p, abort);
-    return;
-  }
+  if (!__all_sync(0xffffffffu, mbar_wait(bar.o_done(t), (done + n_t - 1) & 1, abort, p.timeout_ns)))
+    return false;
   tc_fence_after();
-  // Epilogue: O / l -> bf16 row of the output.
+  // Epilogue: O / l -> bf16 row of the output. The next work tile's first PV
+  // into this O is issued only after this warp's next P is ready, i.e. after
+  // these loads have completed.
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  const bool row_ok = r < g.rows[t];
+  const bool row_ok = r < g.rows_t;
   const int tok = g.q_start + row / p.qpk;
-  const int head = tile.kv_head * p.qpk + row % p.qpk;
+  const int head = g.kv_head * p.qpk + row % p.qpk;
   uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) +
                  (static_cast<int64_t>(tok) * p.num_q_heads + head) * D * 2;
 #pragma unroll
@@ -425,6 +629,43 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const ua_ti
             make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
     }
   }
+  return true;
+}
+
+// Softmax warpgroup of query tile t over the CTA's work tiles.
+template <int D>
+__device__ __forceinline__ void softmax_role(const PrefillParams& p, const uint8_t* ring, int t,
+                                             uint8_t* sV, uint32_t tmem, const Bars<D>& bar,
+                                             volatile int32_t* abort, int warp, int lane) {
+  int done = 0, step = 0;
+  for (int k = 0;; ++k) {
+    Item it;
+    if (!__all_sync(0xffffffffu, take_item<D>(p, bar, ring, k, it, abort))) {
+      give_up(p, abort);
+      return;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar.item_empty(k % kItemSlots));
+    if (it.end) break;
+    SoftmaxTile st;
+    st.kv_head = it.kv_head;
+    st.row0 = it.row0;
+    st.q_start = it.g.q_start;
+    st.ctx = it.g.ctx;
+    st.kv_lo = it.g.kv_lo;
+    st.kv_hi = it.g.kv_hi;
+    st.nmax = it.g.nmax;
+    st.n_t = t ? it.g.ntiles[1] : it.g.ntiles[0];
+    st.rows_t = t ? it.g.rows[1] : it.g.rows[0];
+    if (st.n_t > 0) {
+      if (!softmax_tile<D>(p, st, t, done, step, sV, tmem, bar, abort, warp, lane)) {
+        give_up(p, abort);
+        return;
+      }
+      done += st.n_t;
+    }
+    step += st.nmax;
+  }
 }
 
 template <int D>
@@ -440,53 +681,39 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = sm + L::kQ;
   uint8_t* sK = sm + L::kK;
   uint8_t* sV = sm + L::kV;
-  const Bars bar = bars_at<KS, VS>(reinterpret_cast<uint64_t*>(sm + L::kBar));
+  const Bars<D> bar{smem_u32(sm + L::kBar)};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc);
   volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(sm + L::kMisc + 8);
   volatile int32_t* never = reinterpret_cast<volatile int32_t*>(sm + L::kMisc + 12);
+  uint8_t* ring = sm + L::kItems;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const ua_tile tile = p.tiles[blockIdx.x];
-  // Per-sequence values from the device arrays; ranges are clamped so that
-  // disagreeing host/device lengths cannot send a read out of bounds.
-  Geometry g;
-  g.q_start = p.cu_query_lens[tile.seq];
-  const int qlen = p.cu_query_lens[tile.seq + 1] - g.q_start;
-  const int kv_len = p.kv_lens[tile.seq];
-  g.ctx = kv_len - qlen;
-  g.nrows = min(tile.nrows, qlen * p.qpk - tile.row0);
-  g.kv_hi = min(min(tile.kv_hi, kv_len), p.max_blocks_per_seq * p.block_size);
-  g.kv_lo = tile.kv_lo;
-  g.nmax = 0;
-  for (int t = 0; t < kTilesPerCta; ++t) {
-    g.rows[t] = max(0, min(kRows, g.nrows - t * kRows));
-    g.ntiles[t] = 0;
-    if (g.rows[t] > 0) {
-      const int last = tile.row0 + t * kRows + g.rows[t] - 1;
-      const int hi = p.causal ? min(g.kv_hi, g.ctx + last / p.qpk + 1) : g.kv_hi;
-      g.ntiles[t] = hi > g.kv_lo ? (hi - g.kv_lo + kKeys - 1) / kKeys : 0;
-    }
-    g.nmax = max(g.nmax, g.ntiles[t]);
-  }
 
   if (tid == 0) {
     *abort = 0;
     *never = 0;
-    mbar_init(bar.q_full, 1);
+    for (int t = 0; t < kTilesPerCta; ++t) {
+      mbar_init(bar.q_full(t), 1);
+      mbar_init(bar.q_empty(t), 1);
+    }
     for (int s = 0; s < KS; ++s) {
-      mbar_init(&bar.kfull[s], 1);
-      mbar_init(&bar.kempty[s], 1);
+      mbar_init(bar.kfull(s), 1);
+      mbar_init(bar.kempty(s), 1);
     }
     for (int s = 0; s < VS; ++s) {
-      mbar_init(&bar.vfull[s], 1);
-      mbar_init(&bar.vempty[s], 1);
+      mbar_init(bar.vfull(s), 1);
+      mbar_init(bar.vempty(s), 1);
     }
     for (int t = 0; t < kTilesPerCta; ++t) {
-      mbar_init(&bar.s_full[t], 1);
-      mbar_init(&bar.p_ready[t], kRows);
-      mbar_init(&bar.o_done[t], 1);
+      mbar_init(bar.s_full(t), 1);
+      mbar_init(bar.p_ready(t), kRows);
+      mbar_init(bar.o_done(t), 1);
     }
-    mbar_init(bar.mma_done, 1);
+    mbar_init(bar.mma_done(), 1);
+    for (int s = 0; s < kItemSlots; ++s) {
+      mbar_init(bar.item_full(s), 1);
+      mbar_init(bar.item_empty(s), kItemConsumers);
+    }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -497,20 +724,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
-    if (g.nmax > 0) {
-      if (warp == 0 && lane == 0) {
-        producer_role<D, false>(&map_q, &map_k, p, tile, g, sQ, sK, bar.kfull, bar.kempty, KS,
-                                bar.q_full, abort, never);
-      } else if (warp == 2 && lane == 0) {
-        producer_role<D, true>(&map_q, &map_v, p, tile, g, sQ, sV, bar.vfull, bar.vempty, VS,
-                               bar.q_full, abort, never);
-      } else if (warp == 1 && lane == 0) {
-        mma_role<D>(p, g, sQ, sK, sV, tmem, bar, abort, never);
-      }
+    if (warp == 0 && lane == 0) {
+      producer_role<D, false>(&map_q, &map_k, p, ring, sQ, sK, bar.kfull(0), bar.kempty(0), bar,
+                              abort, never);
+    } else if (warp == 2 && lane == 0) {
+      producer_role<D, true>(&map_q, &map_v, p, ring, sQ, sV, bar.vfull(0), bar.vempty(0), bar,
+                             abort, never);
+    } else if (warp == 1 && lane == 0) {
+      mma_role<D>(p, ring, sQ, sK, sV, tmem, bar, abort, never);
+    } else if (warp == 3 && lane == 0) {
+      scheduler_role<D>(p, bar, ring, abort);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-    if (g.nmax > 0) softmax_role<D>(p, tile, g, (warp - 4) / 4, sV, tmem, bar, abort, warp, lane);
+    softmax_role<D>(p, ring, (warp - 4) / 4, sV, tmem, bar, abort, warp, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -537,7 +764,7 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Smem<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  prefill_kernel<D><<<p.num_tiles, kThreads, Smem<D>::kAlloc, stream>>>(mq, mk, mv, p);
+  prefill_kernel<D><<<p.num_ctas, kThreads, Smem<D>::kAlloc, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -552,7 +779,8 @@ bool prefill_supported(int head_dim, int kv_dtype, int qpk, int block_size) {
 cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_cache,
                            const void* v_cache, int64_t total_q, int head_dim, int num_kv_heads,
                            cudaStream_t stream) {
-  if (p.num_tiles <= 0) return cudaSuccess;
+  if (p.num_tiles <= 0 || p.num_ctas <= 0) return cudaSuccess;
+  if (p.counters == nullptr) return cudaErrorInvalidValue;
   CUtensorMap mq, mk, mv;
   {
     // Q as [total_q][Hq][D]: a box of (64 dims, qpk heads, 128/qpk tokens)

@@ -24,6 +24,7 @@ struct ua_plan {
   ua_combine_group* d_groups = nullptr;
   int32_t* d_err = nullptr;
   int32_t* d_counters = nullptr;   // per combine group, zero between calls
+  int32_t* d_prefill_counters = nullptr;  // [2] persistent prefill tile queue, zero between calls
   float* d_ws = nullptr;           // split workspace: partial rows then lse values
   float* d_ws_o = nullptr;
   float* d_ws_lse = nullptr;
@@ -91,6 +92,8 @@ void fill_info(const ua::Schedule& s, int head_dim, int num_sms, ua_plan_info* i
   info->workspace_bytes = ua::workspace_bytes(s, head_dim);
   info->split_tokens = s.split_tokens;
   info->num_sms = num_sms;
+  info->num_prefill_ctas = s.prefill_ctas;
+  info->reserved = 0;
 }
 
 ua::KernelParams base_params(const ua_plan* plan, const void* q, const void* k, const void* v,
@@ -234,7 +237,8 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   const size_t n_pre = s.prefill.size(), n_dec = s.decode.size(), n_grp = s.groups.size();
   const size_t bytes_tiles = (n_pre + n_dec) * sizeof(ua_tile);
   const size_t bytes_groups = n_grp * sizeof(ua_combine_group);
-  const size_t bytes_meta = bytes_tiles + bytes_groups + 16 + n_grp * sizeof(int32_t);
+  const size_t off_pc = bytes_tiles + bytes_groups + 16 + n_grp * sizeof(int32_t);
+  const size_t bytes_meta = off_pc + 2 * sizeof(int32_t);
   std::vector<uint8_t> host(bytes_meta, 0);
   if (n_pre) std::memcpy(host.data(), s.prefill.data(), n_pre * sizeof(ua_tile));
   if (n_dec) std::memcpy(host.data() + n_pre * sizeof(ua_tile), s.decode.data(),
@@ -252,6 +256,7 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   plan->d_groups = reinterpret_cast<ua_combine_group*>(base + bytes_tiles);
   plan->d_err = reinterpret_cast<int32_t*>(base + bytes_tiles + bytes_groups);
   plan->d_counters = reinterpret_cast<int32_t*>(base + bytes_tiles + bytes_groups + 16);
+  plan->d_prefill_counters = reinterpret_cast<int32_t*>(base + off_pc);
   if (plan->info.workspace_bytes > 0) {
     if (cudaMalloc(&plan->d_ws, static_cast<size_t>(plan->info.workspace_bytes)) != cudaSuccess) {
       free_plan_memory(plan);
@@ -332,6 +337,8 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     std::memset(&pp, 0, sizeof(pp));
     pp.tiles = plan->d_prefill;
     pp.num_tiles = static_cast<int32_t>(s.prefill.size());
+    pp.counters = plan->d_prefill_counters;
+    pp.num_ctas = plan->info.num_prefill_ctas;
     pp.cu_query_lens = cu_query_lens;
     pp.kv_lens = kv_lens;
     pp.block_tables = block_tables;

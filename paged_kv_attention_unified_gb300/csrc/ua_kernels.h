@@ -9,8 +9,10 @@
 namespace ua {
 
 struct PrefillParams {
-  const ua_tile* tiles;
+  const ua_tile* tiles;       // taken in list order by the persistent CTAs
   int32_t num_tiles;
+  int32_t* counters;          // [2] next tile, finished CTAs; zero between launches
+  int32_t num_ctas;           // persistent CTAs (at most one per SM)
   const int32_t* cu_query_lens;
   const int32_t* kv_lens;
   const int32_t* block_tables;
@@ -37,7 +39,8 @@ constexpr int32_t kDebugProducerIdle = 1;
 // (host-only check, no CUDA call).
 bool prefill_supported(int head_dim, int kv_dtype, int qpk, int block_size);
 
-// Prefill kernel over p.tiles (the host encodes the tensor maps from the pointers).
+// Persistent prefill kernel: p.num_ctas CTAs take p.tiles in order as they
+// free up (the host encodes the tensor maps from the pointers).
 cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_cache,
                            const void* v_cache, int64_t total_q, int head_dim,
                            int num_kv_heads, cudaStream_t stream);

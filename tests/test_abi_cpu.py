@@ -159,6 +159,7 @@ def _check_schedule(cu, kv, hq, hkv, causal=1, window=0, num_splits=0, num_sms=1
     # longest-first order
     work = [(t["kv_hi"] - t["kv_lo"]) * t["nrows"] for t in dec]
     assert work == sorted(work, reverse=True)
+    assert info.num_prefill_ctas == min(num_sms, len(pre))
     return info, pre, dec, grp
 
 
@@ -210,3 +211,58 @@ def test_schedule_random_brute_force():
         _check_schedule(cu, kv, hq, hkv, causal=rng.choice([0, 1]), window=rng.choice([0, 0, 9]),
                         num_splits=rng.choice([0, 0, 1, 3, 7]), num_sms=rng.choice([2, 152]),
                         decode_rows_max=rng.choice([-1, 8, 32]))
+
+
+def _prefill_cost(t, cu, kv, qpk, causal=1):
+    """128 x 128 query-key blocks of one prefill tile (both 128-row query tiles)."""
+    s = t["seq"]
+    ql = cu[s + 1] - cu[s]
+    ctx = kv[s] - ql
+    cost = 0
+    for r0 in range(t["row0"], t["row0"] + t["nrows"], 128):
+        rows = min(128, t["row0"] + t["nrows"] - r0)
+        hi = min(kv[s], ctx + (r0 + rows - 1) // qpk + 1) if causal else kv[s]
+        cost += max(0, -(-(hi - t["kv_lo"]) // 128))
+    return cost
+
+
+@pytest.mark.parametrize("case", ["dense", "mixed"])
+def test_prefill_list_ends_with_shortest_tiles(case):
+    """The persistent prefill CTAs take tiles in list order: the shortest tiles,
+    up to 1/16 of the work, come last and longest first; the rest keeps the
+    (sequence, KV head) grouping."""
+    if case == "dense":
+        cu, kv, hq, hkv = [0, 4096, 8192, 12288, 16384], [4096] * 4, 32, 32
+    else:
+        rng = np.random.default_rng(3)
+        ql = [int(x) for x in rng.integers(512, 2049, 8)] + [1] * 20
+        kv = [q + int(c) for q, c in zip(ql[:8], rng.integers(0, 1025, 8))] + \
+             [int(x) for x in rng.integers(1024, 8193, 20)]
+        cu = [0] + list(np.cumsum(ql))
+        hq, hkv = 32, 8
+    cu = [int(x) for x in cu]
+    info, pre, dec, grp = ua.ua_schedule(cu, kv, hq, hkv, 128, 16, max(kv) // 16 + 2)
+    qpk = hq // hkv
+    cost = [_prefill_cost(t, cu, kv, qpk) for t in pre]
+    total = sum(cost)
+    # size of the tail: the shortest tiles whose cost adds up to at most 1/16
+    m, acc = 0, 0
+    for c in sorted(cost):
+        if acc + c > total / 16:
+            break
+        acc += c
+        m += 1
+    assert 0 < m < len(pre)
+    tail, bulk = cost[len(pre) - m:], cost[:len(pre) - m]
+    assert tail == sorted(tail, reverse=True)
+    assert max(tail) <= min(bulk)
+    assert sum(tail) <= total / 16
+    # the bulk keeps each (sequence, KV head) group contiguous
+    seen, prev = set(), None
+    for t in pre[:len(pre) - m]:
+        key = (t["seq"], t["kv_head"])
+        if key != prev:
+            assert key not in seen
+            seen.add(key)
+            prev = key
+    assert info.num_prefill_ctas == min(152, len(pre))
