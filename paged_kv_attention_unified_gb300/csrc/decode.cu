@@ -73,6 +73,34 @@ __device__ __forceinline__ int v_dim(int v, int g) {
   return (v / C::VE) * 8 * C::VE + g * C::VE + (v % C::VE);
 }
 
+// Shared-memory layout of one 16-key page of K or V as TMA lands it. Rows of
+// at least 128 bytes arrive as 128-byte-wide panels (16 rows each) with the
+// 128-byte swizzle: the 16-byte chunk c of row r sits at chunk c ^ (r % 8).
+// The fragment reads below touch 8 rows at one column (K) or 4 whole rows (V)
+// per instruction; with the swizzle both take the minimum of 4 wavefronts
+// (unswizzled, the 8 K rows at a 256-byte stride share half of the banks).
+// The e4m3 path keeps plain rows: its K reads are half as many and its
+// conversion work leaves no issue slots for the swizzled address arithmetic
+// (measured: slower with the swizzle).
+template <int D, bool FP8>
+struct PageLayout {
+  static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
+  static constexpr bool kSwizzle = !FP8 && kRowBytes >= 128;
+  static constexpr int kBoxDims = kSwizzle ? 128 / (FP8 ? 1 : 2) : D;  // elements per box row
+  static constexpr int kPanels = kSwizzle ? kRowBytes / 128 : 1;
+  static constexpr int kPanelBytes = 16 * (kSwizzle ? 128 : kRowBytes);
+  // Byte address of row `key`, byte `o` of the row (o a multiple of 8).
+  __device__ static __forceinline__ int at(int key, int o) {
+    if constexpr (kSwizzle) {
+      const int within = o & 127;
+      return (o >> 7) * kPanelBytes + key * 128 + ((((within >> 4) ^ (key & 7))) << 4) +
+             (within & 15);
+    } else {
+      return key * kRowBytes + o;
+    }
+  }
+};
+
 template <int D, bool FP8>
 struct StepRegs {
   uint32_t k[2][DecodeCfg<D, FP8>::KW];   // K rows key_of_row(g), key_of_row(g+8)
@@ -86,16 +114,16 @@ template <int D, bool FP8>
 __device__ __forceinline__ void read_step(StepRegs<D, FP8>& r, const uint8_t* kp,
                                           const uint8_t* vp, int base, int kv_hi, int g, int t) {
   using C = DecodeCfg<D, FP8>;
-  constexpr int kRowBytes = D * C::ELT;
+  using PL = PageLayout<D, FP8>;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int key = key_of_row(g + 8 * h);
     const bool ok = base + key < kv_hi;
-    const uint8_t* row = kp + key * kRowBytes;
 #pragma unroll
     for (int l = 0; l < C::NKL; ++l) {
       uint4 x = make_uint4(0u, 0u, 0u, 0u);
-      if (ok) x = *reinterpret_cast<const uint4*>(row + (l * 4 * C::KE + t * C::KE) * C::ELT);
+      if (ok)
+        x = *reinterpret_cast<const uint4*>(kp + PL::at(key, (l * 4 * C::KE + t * C::KE) * C::ELT));
       r.k[h][4 * l + 0] = x.x;
       r.k[h][4 * l + 1] = x.y;
       r.k[h][4 * l + 2] = x.z;
@@ -106,10 +134,9 @@ __device__ __forceinline__ void read_step(StepRegs<D, FP8>& r, const uint8_t* kp
   for (int j = 0; j < 4; ++j) {
     const int key = 4 * t + j;
     const bool ok = base + key < kv_hi;
-    const uint8_t* row = vp + key * kRowBytes;
 #pragma unroll
     for (int l = 0; l < C::NVL; ++l) {
-      const uint8_t* a = row + (l * 8 * C::VE + g * C::VE) * C::ELT;
+      const uint8_t* a = vp + PL::at(key, (l * 8 * C::VE + g * C::VE) * C::ELT);
       if constexpr (C::VLB == 16) {
         uint4 x = make_uint4(0u, 0u, 0u, 0u);
         if (ok) x = *reinterpret_cast<const uint4*>(a);
@@ -234,9 +261,10 @@ __device__ __forceinline__ void compute_step(WarpState<D>& st, const StepRegs<D,
 }
 
 // Shared memory of one CTA: a ring of R stages per warp, each holding the K
-// and V rows (16 x head_dim) of one 16-key step as TMA lands them; then one
-// mbarrier per stage. After the loop the ring is reused for the cross-warp
-// merge. About 64 KB, so that three CTAs (twelve warps) share an SM.
+// and V rows (16 x head_dim, in the page layout above) of one 16-key step as
+// TMA lands them; then one mbarrier per stage. After the loop the ring is
+// reused for the cross-warp merge. About 64 KB, so that three CTAs (twelve
+// warps) share an SM.
 template <int D, bool FP8>
 struct Ring {
   static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
@@ -246,7 +274,7 @@ struct Ring {
   static constexpr int kBars = kRing;
   static constexpr int kMisc = kBars + 8 * kWarps * kStages;
   static constexpr int kBytes = kMisc + 16;
-  static constexpr int kAlloc = kBytes + 128;  // slack for 128-byte alignment
+  static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment (swizzle atoms)
   static_assert(kWarps * UA_DECODE_ROWS * (D + 2) * 4 <= kRing, "merge buffers alias the ring");
 };
 
@@ -259,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   constexpr int R = RC::kStages;
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(dsm_raw) + 127) & ~static_cast<uintptr_t>(127));
+      (reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + RC::kBars);
   volatile int32_t* never = reinterpret_cast<volatile int32_t*>(dsm + RC::kMisc);
   // merge buffers (valid only after the loop; they alias the ring)
@@ -404,9 +432,14 @@ __global__ void __launch_bounds__(kThreads, 3)
       uint8_t* stage = ring + st * RC::kStage;
       sm100::fence_proxy_async_smem();
       sm100::mbar_arrive_expect_tx(&wbar[st], RC::kStage);
-      sm100::tma_load_4d(stage, &map_k, &wbar[st], 0, tile.kv_head, base % p.block_size, blk);
-      sm100::tma_load_4d(stage + 16 * RC::kRowBytes, &map_v, &wbar[st], 0, tile.kv_head,
-                         base % p.block_size, blk);
+      using PL = PageLayout<D, FP8>;
+#pragma unroll
+      for (int pn = 0; pn < PL::kPanels; ++pn) {
+        sm100::tma_load_4d(stage + pn * PL::kPanelBytes, &map_k, &wbar[st], pn * PL::kBoxDims,
+                           tile.kv_head, base % p.block_size, blk);
+        sm100::tma_load_4d(stage + 16 * RC::kRowBytes + pn * PL::kPanelBytes, &map_v, &wbar[st],
+                           pn * PL::kBoxDims, tile.kv_head, base % p.block_size, blk);
+      }
     }
   };
   int issued = 0, done = 0;
@@ -564,12 +597,14 @@ template <int D, bool FP8>
 cudaError_t launch_decode_d(const KernelParams& p, cudaStream_t stream) {
   CUtensorMap mk, mv;
   const int elt = FP8 ? 1 : 2;
-  // one box = the 16 key rows (all head dims) of one KV head in one page
+  using PL = PageLayout<D, FP8>;
+  // one box = the 16 key rows of one KV head in one page, one 128-byte panel
+  // of head dims (swizzled) or the whole row
   cudaError_t e = encode_kv_page_map(&mk, p.k_cache, elt, D, p.num_kv_heads, p.block_size,
-                                     p.num_blocks, D, 16, false);
+                                     p.num_blocks, PL::kBoxDims, 16, PL::kSwizzle);
   if (e == cudaSuccess)
-    e = encode_kv_page_map(&mv, p.v_cache, elt, D, p.num_kv_heads, p.block_size, p.num_blocks, D,
-                           16, false);
+    e = encode_kv_page_map(&mv, p.v_cache, elt, D, p.num_kv_heads, p.block_size, p.num_blocks,
+                           PL::kBoxDims, 16, PL::kSwizzle);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(decode_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Ring<D, FP8>::kAlloc);
