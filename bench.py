@@ -239,6 +239,34 @@ def _rate(cfg, byts, flops, seconds):
     return (flops / seconds / 1e12) if cfg == 4 else (byts / seconds / 1e9)
 
 
+# ---- replicas across ranks (weak scaling: an independent batch per GPU) ----
+
+def rank_case(cfg, rank):
+    """This rank's batch: the workload drawn with seed = rank."""
+    import workloads as W
+    return W.CONFIGS[cfg](seed=rank)
+
+
+def max_over_ranks(value, world, device="cpu"):
+    """Largest value over the ranks (the job's step time is its slowest rank's)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value, world, device="cpu"):
+    """Sum over the ranks (work units the whole job processed)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
 def run_reference(args):
     """The oracle as the reference arm: host cores only, rank 0 only."""
     if int(os.environ.get("RANK", "0")) != 0:
@@ -306,7 +334,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     B.build()
     cfg = args.workload
-    case = W.CONFIGS[cfg](seed=rank)            # weak scaling: one batch per GPU
+    case = rank_case(cfg, rank)                 # weak scaling: one batch per GPU
     byts, flops = algorithmic_work(case)
     metric, unit = _metric_for(cfg)
     hbm_peak, tf_peak, peak_src = _peaks()
@@ -361,12 +389,11 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     ktimes = ua.ua_plan_kernel_times(plan.handle)
-    ms_t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ms, world, device="cuda")
     step_s = ms_max / 1e3 / args.steps
-    value = _rate(cfg, byts * world, flops * world, step_s)
+    job_bytes = sum_over_ranks(byts, world, device="cuda")
+    job_flops = sum_over_ranks(flops, world, device="cuda")
+    value = _rate(cfg, job_bytes, job_flops, step_s)
 
     # dominant kernel and its roofline, credited with the work of the sequences
     # the scheduler gave it (host-only schedule of the same batch)

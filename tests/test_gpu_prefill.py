@@ -77,6 +77,29 @@ def test_mixed_prefill_and_decode_in_one_plan():
     _check(case, decode_rows_max=32)
 
 
+def test_more_tiles_than_ctas_and_repeated_forwards():
+    """320 prefill tiles for at most one CTA per SM: CTAs run several tiles in
+    a row (rings and barrier phases carry over), and the tile queue re-arms
+    between forwards, so three forwards on one plan give the same bits."""
+    rng = np.random.default_rng(280)
+    ql = [64] * 40
+    kv = [64 + int(c) for c in rng.integers(0, 300, 40)]
+    case = W.make_case("many_tiles", ql, kv, 32, 8, 128, 16, seed=280)
+    b = tu.to_device(case)
+    with tu.make_plan(b, decode_rows_max=0) as plan:
+        info = plan.info
+        assert info.num_prefill_tiles == 320
+        assert info.num_prefill_ctas == min(info.num_sms, 320)
+        outs = []
+        for _ in range(3):
+            outs.append(tu.forward(plan, b))
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
+    assert_close(as_f64(outs[0]), oracle_full(case), case.kv_dtype, case.name)
+
+
 def test_block_permutation_gives_identical_bits():
     case = W.make_case("perm", [500, 200], [800, 333], 8, 2, 128, 16, seed=280)
     b = tu.to_device(case)
