@@ -56,7 +56,7 @@ def _rank_main(rank, world, port, results):
 def test_two_rank_replicas_gloo():
     world = 2
     port = _free_port()
-    with mp.Manager() as mgr:
+    with mp.get_context("spawn").Manager() as mgr:
         results = mgr.dict()
         mp.spawn(_rank_main, args=(world, port, results), nprocs=world, join=True)
         res = dict(results)
