@@ -25,8 +25,11 @@ kernel_unified_attention_2d sections):
 Inputs are raw bit patterns (bf16 words as uint16, e4m3 codes as uint8) and
 are widened to fp64 exactly from their format definitions.
 
-Parity pins live in tests/test_oracle_pins.py; every function below is pinned
-there (none is "parity unpinned").
+The append step (writing a step's new K/V into the paged cache, with the
+e4m3 quantisation of the fp8 cache) is in oracle/append.py.
+
+Parity pins live in tests/test_oracle_pins.py and tests/test_append_pins.py;
+every function is pinned there (none is "parity unpinned").
 """
 from .attention import (  # noqa: F401
     decode_bf16,
@@ -40,3 +43,4 @@ from .attention import (  # noqa: F401
     partial_attention,
     combine_partials,
 )
+from .append import encode_e4m3, quantize_e4m3, append_kv  # noqa: F401
