@@ -278,6 +278,8 @@ def run_reference(args):
     case = W.CONFIGS[cfg]()
     metric, unit = _metric_for(cfg)
     step_budget = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    if getattr(args, "op", "attention") == "append":
+        return _reference_append(args, case, step_budget)
     with concurrent.futures.ProcessPoolExecutor(
             max_workers=1, mp_context=mp.get_context("spawn")) as ex:
         res = ex.submit(_oracle_steps_worker, cfg, args.warmup + args.steps, step_budget).result()
@@ -486,6 +488,191 @@ def run_ours(args):
     return 0
 
 
+def _reference_append(args, case, step_budget):
+    """Reference arm of --op append: the oracle's append, rank 0, host cores."""
+    import concurrent.futures
+    import multiprocessing as mp
+    cfg = args.workload
+    row = case.num_kv_heads * case.head_dim
+    elt = 1 if case.kv_dtype == "fp8_e4m3" else 2
+    toks, spent = 0, 0.0
+    with concurrent.futures.ProcessPoolExecutor(
+            max_workers=1, mp_context=mp.get_context("spawn")) as ex:
+        for k in range(args.warmup + args.steps):
+            t, sp = ex.submit(_oracle_append_worker, cfg, step_budget).result()
+            if k >= args.warmup:
+                toks, spent = toks + t, spent + sp
+    value = 2 * toks * row * (2 + elt) / spent / 1e9
+    sample = (f"each step: the oracle's append over consecutive whole sequences for about "
+              f"{step_budget:.1f} s of single-thread work")
+    line = {
+        "impl": "reference", "metric": "append-KV GB/s (algorithmic new K/V bytes read + cache "
+        "bytes written / step time)", "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * spent / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (CPU oracle)", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": WORKLOAD_NAMES[cfg], "op": "append_kv",
+                   "parallelism": "host, 1 thread"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- append-KV (writing the step's new K/V into the paged cache) ----
+
+def append_work(case):
+    """Bytes one append moves: the new K and V rows read (bf16) and written
+    (cache element size), plus cu_query_lens, kv_lens and one page-table entry
+    per new token."""
+    elt = 1 if case.kv_dtype == "fp8_e4m3" else 2
+    T = int(case.cu_query_lens[-1])
+    row = case.num_kv_heads * case.head_dim
+    return 2 * T * row * (2 + elt) + 4 * (2 * case.num_seqs + 1) + 4 * T
+
+
+def _new_kv(case, seed=1):
+    import torch
+    g = torch.Generator().manual_seed(seed)
+    T = int(case.cu_query_lens[-1])
+    shape = (T, case.num_kv_heads, case.head_dim)
+    return (torch.randn(shape, generator=g).to(torch.bfloat16),
+            torch.randn(shape, generator=g).to(torch.bfloat16))
+
+
+def _oracle_append_worker(cfg, budget_s):
+    """Spawned process, one thread: the oracle's append over consecutive
+    sequences of the workload for about budget_s. Returns (tokens, seconds)."""
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    import numpy as np
+    import oracle
+    import workloads as W
+    case = W.CONFIGS[cfg]()
+    r = case.raw()
+    kn, vn = _new_kv(case)
+    kn = kn.view(__import__("torch").int16).numpy().view(np.uint16)
+    vn = vn.view(__import__("torch").int16).numpy().view(np.uint16)
+    cu = r["cu_query_lens"]
+    toks, spent, s = 0, 0.0, 0
+    while spent < budget_s and s < case.num_seqs:
+        t0 = time.perf_counter()
+        oracle.append_kv(kn[cu[s]:cu[s + 1]], vn[cu[s]:cu[s + 1]], r["k_cache"], r["v_cache"],
+                         [0, int(cu[s + 1] - cu[s])], r["kv_lens"][s:s + 1],
+                         r["block_tables"][s:s + 1], case.block_size, kv_dtype=case.kv_dtype,
+                         k_scale=case.k_scale, v_scale=case.v_scale)
+        spent += time.perf_counter() - t0
+        toks += int(cu[s + 1] - cu[s])
+        s += 1
+    return toks, spent
+
+
+def run_append(args):
+    """One step = ua_append_kv of every new token of the workload's batch (the
+    q tokens' K and V) into its paged cache; HBM-bound."""
+    import torch
+    import concurrent.futures
+    import multiprocessing as mp
+    import paged_kv_attention_unified_gb300 as ua
+    from paged_kv_attention_unified_gb300 import build as B
+    from paged_kv_attention_unified_gb300 import torch_utils as tu
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    B.build()
+    cfg = args.workload
+    case = rank_case(cfg, rank)
+    byts = append_work(case)
+    hbm_peak, _, peak_src = _peaks()
+    T = int(case.cu_query_lens[-1])
+    row = case.num_kv_heads * case.head_dim
+    elt = 1 if case.kv_dtype == "fp8_e4m3" else 2
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        with concurrent.futures.ProcessPoolExecutor(
+                max_workers=1, mp_context=mp.get_context("spawn")) as ex:
+            toks, spent = ex.submit(_oracle_append_worker, cfg, args.cpu_budget).result()
+        cpu_b = 2 * toks * row * (2 + elt)
+        cpu = {"value": cpu_b / spent / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{toks} of {T} new tokens (whole sequences), {spent:.1f} s of "
+                         "single-thread fp64-oracle work"}
+    b = tu.to_device(case)
+    kn, vn = (t.cuda() for t in _new_kv(case))
+    plan = tu.make_plan(b)
+    ua.ua_plan_set_profiling(plan.handle, True)
+    for _ in range(args.warmup):
+        tu.append_kv(plan, b, kn, vn)
+    torch.cuda.synchronize()
+    ua.ua_plan_kernel_times(plan.handle)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    ms = 0.0
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            tu.append_kv(plan, b, kn, vn)
+            t1.record(stream)
+            torch.cuda.synchronize()
+            ms += t0.elapsed_time(t1)
+    kt = ua.ua_plan_kernel_times(plan.handle)["append"]
+    ms_max = max_over_ranks(ms, world, device="cuda")
+    job_bytes = sum_over_ranks(byts, world, device="cuda")
+    value = job_bytes / (ms_max / 1e3 / args.steps) / 1e9
+    avg_s = kt[0] / 1e3 / max(1, kt[1])
+    ach = byts / avg_s / 1e9
+    roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+            "frac": ach / hbm_peak, "work_per_launch": byts, "kernel": "append",
+            "kernel_avg_us": avg_s * 1e6, "kernel_share": 1.0,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured"
+            else "fallback",
+            "traffic": _traffic_record("append", cfg)[0]}
+    # end to end: pinned host K/V rows -> device, append, read the error word
+    kh, vh = kn.cpu().pin_memory(), vn.cpu().pin_memory()
+    tot = 0.0
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t_0 = time.perf_counter()
+        kn.copy_(kh, non_blocking=True)
+        vn.copy_(vh, non_blocking=True)
+        tu.append_kv(plan, b, kn, vn)
+        err = plan.last_device_error()
+        if it >= args.warmup:
+            tot += time.perf_counter() - t_0
+    assert err == 0
+    plan.close()
+    if rank != 0:
+        return 0
+    line = {
+        "metric": "append-KV GB/s (algorithmic new K/V bytes read + cache bytes written / step time)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 -> fp8 e4m3 (x / scale, saturating)" if elt == 1 else "bf16 copy",
+        "data": "synthetic (seeded N(0,1), random page tables)",
+        "config": {"workload": WORKLOAD_NAMES[cfg], "op": "append_kv", "new_tokens": T,
+                   "l2": "L2 flushed (256 MB write) between timed steps",
+                   "parallelism": "replicas: an independent batch per GPU, no collective"},
+        "algorithmic": {"bytes_per_step": byts},
+        "pct_of_peak": (value / world) / hbm_peak,
+        "roofline": roof, "cpu_baseline": cpu,
+        "e2e": {"value": byts / (tot / args.steps) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(kh.numel() * 2 * 2), "d2h_bytes_per_step": 4,
+                "includes": "H2D of the new K/V rows, append, read of the error word"},
+        "gpu_launches": int(kt[1]), "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -497,11 +684,16 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", default="attention", choices=["attention", "append"],
+                    help="attention: the forward step (default); append: ua_append_kv of the "
+                         "step's new K/V")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "append":
+        return run_append(args)
     return run_ours(args)
 
 

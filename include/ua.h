@@ -201,14 +201,43 @@ ua_status ua_forward_oneshot(const void* q, const void* k_cache, const void* v_c
                              float k_scale, float v_scale, int32_t num_splits,
                              ua_stream_t stream);
 
+/*
+ * ua_append_kv -- write a step's new keys and values into the paged cache
+ * (the Append_KV path of the split-KV launcher in "flashatten takeaways EP2
+ * 工程"), before ua_forward reads them. For sequence s of the plan and new
+ * token i < q_len_s (row cu_query_lens[s] + i of k_new / v_new), logical
+ * position pos = kv_len_s - q_len_s + i is written at block
+ * block_tables[s][pos / block_size], slot pos % block_size, all KV heads.
+ * The positions come from the lengths the plan was built with (one tile of
+ * up to 8 new tokens per CTA, listed by the plan).
+ * k_new, v_new: device [total_q, num_kv_heads, head_dim] bf16 (the plan's
+ *   total_q = cu_query_lens_host[num_seqs]), contiguous, 16-byte aligned.
+ * k_cache, v_cache: the caches of ua_forward (written in place).
+ * block_tables: the device page table (as for ua_forward).
+ * fp8 (e4m3) cache: code = e4m3(x / k_scale) (v_scale for V), the quotient
+ *   in binary32, rounded to nearest even, saturating at +-448, NaN stays NaN;
+ *   the scales must be finite and non-zero. bf16 cache: a copy (scales
+ *   ignored).
+ * A page id outside [0, num_blocks) (or a position past the page table) is
+ * not written; UA_ERR_BOUNDS is recorded in the plan's error word.
+ * Stream-ordered on `stream`; issue it before ua_forward on the same stream.
+ * Returns UA_ERR_INVALID_ARG for null or misaligned pointers, a bad
+ * num_blocks or scale, or a stream on another device than the plan's.
+ */
+ua_status ua_append_kv(const ua_plan* plan, const void* k_new, const void* v_new, void* k_cache,
+                       void* v_cache, const int32_t* block_tables, int64_t num_blocks,
+                       float k_scale, float v_scale, ua_stream_t stream);
+
 /* Counts and sizes of a plan (host memory only). */
 ua_status ua_plan_get_info(const ua_plan* plan, ua_plan_info* info);
 
-/* Kernel timing for measurement tools. While enabled, ua_forward records a
- * CUDA event pair on its stream around each kernel launch (negligible cost);
- * ua_plan_kernel_times synchronises, sums the elapsed milliseconds and launch
- * counts per kernel kind since the last read -- index 0 prefill, 1 decode,
- * 2 combine -- into ms[0..2] / launches[0..2], and clears them. */
+/* Kernel timing for measurement tools. While enabled, ua_forward and
+ * ua_append_kv record a CUDA event pair on their stream around each kernel
+ * launch (a few microseconds per launch); ua_plan_kernel_times synchronises,
+ * sums the elapsed milliseconds and launch counts per kernel kind since the
+ * last read -- index 0 prefill, 1 decode, 2 combine, 3 append -- into
+ * ms[0..UA_KERNEL_KINDS-1] / launches[0..UA_KERNEL_KINDS-1], and clears them. */
+#define UA_KERNEL_KINDS 4
 ua_status ua_plan_set_profiling(ua_plan* plan, int32_t enable);
 ua_status ua_plan_kernel_times(ua_plan* plan, float* ms, int64_t* launches);
 

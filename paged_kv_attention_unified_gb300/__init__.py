@@ -33,7 +33,7 @@ EXPORTS = (
     "ua_schedule", "ua_plan_create", "ua_plan_create_ex", "ua_forward", "ua_forward_oneshot",
     "ua_plan_get_info", "ua_last_device_error", "ua_plan_destroy", "ua_status_string",
     "ua_gather_kv_debug", "ua_plan_set_profiling", "ua_plan_kernel_times",
-    "ua_forward_static_scratch", "ua_plan_set_debug",
+    "ua_forward_static_scratch", "ua_plan_set_debug", "ua_append_kv",
 )
 
 
@@ -80,6 +80,7 @@ _SIGS = {
     "ua_plan_create_ex": (_I32, [ctypes.POINTER(_P), _I32P, _I32P, _I32, _I32, _I32, _I32, _I32,
                                  _I32, _I32, _I32, _I32, _I32, _I32, _P]),
     "ua_forward": (_I32, [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I32, _I32, _F, _F, _F, _P]),
+    "ua_append_kv": (_I32, [_P, _P, _P, _P, _P, _P, _I64, _F, _F, _P]),
     "ua_forward_oneshot": (_I32, [_P, _P, _P, _P, _I32P, _I32P, _P, _P, _P, _I32, _I32, _I32,
                                   _I32, _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32, _I32, _F,
                                   _F, _I32, _P]),
@@ -189,6 +190,17 @@ def ua_forward(plan, q, k_cache, v_cache, out, cu_query_lens, kv_lens, block_tab
                             float(v_scale), _stream_handle(stream)), "ua_forward")
 
 
+def ua_append_kv(plan, k_new, v_new, k_cache, v_cache, block_tables, num_blocks, k_scale=1.0,
+                 v_scale=1.0, stream=None):
+    """Write the step's new K/V rows into the paged cache on `stream` (positions
+    from the plan's lengths). Tensor arguments are CUDA tensors (or raw device
+    pointers)."""
+    ptr = lambda t: t if isinstance(t, int) else t.data_ptr()
+    _check(lib().ua_append_kv(plan, ptr(k_new), ptr(v_new), ptr(k_cache), ptr(v_cache),
+                              ptr(block_tables), int(num_blocks), float(k_scale),
+                              float(v_scale), _stream_handle(stream)), "ua_append_kv")
+
+
 def ua_forward_oneshot(q, k_cache, v_cache, out, cu_query_lens_host, kv_lens_host,
                        cu_query_lens, kv_lens, block_tables, num_q_heads, num_kv_heads,
                        head_dim, block_size, max_blocks_per_seq, num_blocks, kv_dtype, max_q,
@@ -233,13 +245,13 @@ def ua_plan_set_debug(plan: int, flags: int, wait_timeout_ns: int = 0):
     _check(lib().ua_plan_set_debug(plan, int(flags), int(wait_timeout_ns)), "ua_plan_set_debug")
 
 
-KERNEL_KINDS = ("prefill", "decode", "combine")
+KERNEL_KINDS = ("prefill", "decode", "combine", "append")
 
 
 def ua_plan_kernel_times(plan: int):
     """{kind: (milliseconds, launches)} since the last read (synchronises)."""
-    ms = (ctypes.c_float * 3)()
-    n = (ctypes.c_int64 * 3)()
+    ms = (ctypes.c_float * len(KERNEL_KINDS))()
+    n = (ctypes.c_int64 * len(KERNEL_KINDS))()
     _check(lib().ua_plan_kernel_times(plan, ms, n), "ua_plan_kernel_times")
     return {k: (ms[i], n[i]) for i, k in enumerate(KERNEL_KINDS)}
 
@@ -274,6 +286,9 @@ class Plan:
 
     def forward(self, *args, **kwargs):
         ua_forward(self.handle, *args, **kwargs)
+
+    def append_kv(self, *args, **kwargs):
+        ua_append_kv(self.handle, *args, **kwargs)
 
     def last_device_error(self) -> int:
         return ua_last_device_error(self.handle)

@@ -98,6 +98,25 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
     }
   }
 
+  // Append tiles: each sequence's new tokens in runs of kAppendTokens.
+  for (int32_t q = 0; q < p.num_seqs; ++q) {
+    const int32_t q0 = p.cu_query_lens[q];
+    const int32_t ql = p.cu_query_lens[q + 1] - q0;
+    const int32_t ctx = p.kv_lens[q] - ql;
+    for (int32_t j = 0; j < ql; j += kAppendTokens) {
+      ua_tile t;
+      t.seq = q;
+      t.kv_head = 0;
+      t.row0 = q0 + j;
+      t.nrows = std::min(kAppendTokens, ql - j);
+      t.kv_lo = ctx + j;
+      t.kv_hi = t.kv_lo + t.nrows;
+      t.slot = -1;
+      t.group = -1;
+      s.append.push_back(t);
+    }
+  }
+
   // 2. Split-KV for decode tiles (FlashDecoding): one chunk length C for the
   // whole batch, so that pieces are equal-sized and load-balance well.
   int64_t total = 0, longest = 0;

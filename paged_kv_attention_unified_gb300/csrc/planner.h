@@ -38,6 +38,10 @@ struct Schedule {
   std::vector<ua_tile> prefill;
   int32_t prefill_ctas = 0;  // persistent prefill CTAs: min(SMs, prefill tiles)
   std::vector<ua_tile> decode;
+  // Append-KV tiles: up to kAppendTokens consecutive new tokens of one
+  // sequence: seq, row0 = first token (row of k_new), nrows = tokens,
+  // kv_lo = logical cache position of the first token, kv_hi = kv_lo + nrows.
+  std::vector<ua_tile> append;
   std::vector<ua_combine_group> groups;
   int64_t num_slots = 0;
   int32_t split_tokens = 0;
@@ -61,6 +65,8 @@ constexpr int kDefaultDecodeRowsMax = 32;
 constexpr int kPrefillKeyTile = 128;
 // Rows of one tcgen05 query tile of the prefill kernel (two per prefill tile).
 constexpr int kPrefillQueryTile = 128;
+// New tokens per append tile (one warp each in the append kernel).
+constexpr int kAppendTokens = 8;
 // Share of the prefill work (in 128 x 128 query-key blocks) kept for the end
 // of the prefill list: the shortest tiles, so that the CTAs finish together.
 constexpr double kPrefillTailShare = 1.0 / 16.0;

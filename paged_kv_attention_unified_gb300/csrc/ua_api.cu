@@ -25,6 +25,7 @@ struct ua_plan {
   int32_t* d_err = nullptr;
   int32_t* d_counters = nullptr;   // per combine group, zero between calls
   int32_t* d_prefill_counters = nullptr;  // [2] persistent prefill tile queue, zero between calls
+  ua_tile* d_append = nullptr;            // append-KV tiles
   float* d_ws = nullptr;           // split workspace: partial rows then lse values
   float* d_ws_o = nullptr;
   float* d_ws_lse = nullptr;
@@ -238,12 +239,15 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   const size_t bytes_tiles = (n_pre + n_dec) * sizeof(ua_tile);
   const size_t bytes_groups = n_grp * sizeof(ua_combine_group);
   const size_t off_pc = bytes_tiles + bytes_groups + 16 + n_grp * sizeof(int32_t);
-  const size_t bytes_meta = off_pc + 2 * sizeof(int32_t);
+  const size_t n_app = s.append.size();
+  const size_t off_app = (off_pc + 2 * sizeof(int32_t) + 15) & ~static_cast<size_t>(15);
+  const size_t bytes_meta = off_app + n_app * sizeof(ua_tile);
   std::vector<uint8_t> host(bytes_meta, 0);
   if (n_pre) std::memcpy(host.data(), s.prefill.data(), n_pre * sizeof(ua_tile));
   if (n_dec) std::memcpy(host.data() + n_pre * sizeof(ua_tile), s.decode.data(),
                          n_dec * sizeof(ua_tile));
   if (n_grp) std::memcpy(host.data() + bytes_tiles, s.groups.data(), bytes_groups);
+  if (n_app) std::memcpy(host.data() + off_app, s.append.data(), n_app * sizeof(ua_tile));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (cudaMalloc(&plan->d_meta, bytes_meta) != cudaSuccess) {
     free_plan_memory(plan);
@@ -257,6 +261,7 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   plan->d_err = reinterpret_cast<int32_t*>(base + bytes_tiles + bytes_groups);
   plan->d_counters = reinterpret_cast<int32_t*>(base + bytes_tiles + bytes_groups + 16);
   plan->d_prefill_counters = reinterpret_cast<int32_t*>(base + off_pc);
+  plan->d_append = reinterpret_cast<ua_tile*>(base + off_app);
   if (plan->info.workspace_bytes > 0) {
     if (cudaMalloc(&plan->d_ws, static_cast<size_t>(plan->info.workspace_bytes)) != cudaSuccess) {
       free_plan_memory(plan);
@@ -375,6 +380,48 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
   return UA_OK;
 }
 
+ua_status ua_append_kv(const ua_plan* plan, const void* k_new, const void* v_new, void* k_cache,
+                       void* v_cache, const int32_t* block_tables, int64_t num_blocks,
+                       float k_scale, float v_scale, ua_stream_t stream) {
+  if (plan == nullptr) return UA_ERR_INVALID_ARG;
+  if (plan->sched.append.empty()) return UA_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !block_tables) return UA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return UA_ERR_INVALID_ARG;
+  if (num_blocks <= 0 || num_blocks >= INT32_MAX) return UA_ERR_INVALID_ARG;
+  const bool fp8 = plan->prob.kv_dtype == UA_KV_FP8_E4M3;
+  if (fp8 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f ||
+              v_scale == 0.f))
+    return UA_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return UA_ERR_CUDA;
+  if (dev != plan->device) return UA_ERR_INVALID_ARG;
+  ua::AppendParams ap;
+  std::memset(&ap, 0, sizeof(ap));
+  ap.k_new = k_new;
+  ap.v_new = v_new;
+  ap.k_cache = k_cache;
+  ap.v_cache = v_cache;
+  ap.tiles = plan->d_append;
+  ap.num_tiles = static_cast<int32_t>(plan->sched.append.size());
+  ap.block_tables = block_tables;
+  ap.err = plan->d_err;
+  ap.num_blocks = num_blocks;
+  ap.row_elems = plan->prob.num_kv_heads * plan->prob.head_dim;
+  ap.max_blocks_per_seq = plan->prob.max_blocks_per_seq;
+  ap.block_size = plan->prob.block_size;
+  ap.fp8 = fp8 ? 1 : 0;
+  ap.k_scale = k_scale;
+  ap.v_scale = v_scale;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  ua_plan* mp = const_cast<ua_plan*>(plan);
+  mp->last_stream = cs;
+  auto* ev = timing_begin(mp, 3, cs);
+  if (ua::launch_append(ap, cs) != cudaSuccess) return UA_ERR_CUDA;
+  timing_end(ev, cs);
+  return UA_OK;
+}
+
 ua_status ua_forward_oneshot(const void* q, const void* k_cache, const void* v_cache, void* out,
                              const int32_t* cu_query_lens_host, const int32_t* kv_lens_host,
                              const int32_t* cu_query_lens, const int32_t* kv_lens,
@@ -455,7 +502,7 @@ ua_status ua_plan_set_profiling(ua_plan* plan, int32_t enable) {
 
 ua_status ua_plan_kernel_times(ua_plan* plan, float* ms, int64_t* launches) {
   if (plan == nullptr || ms == nullptr || launches == nullptr) return UA_ERR_INVALID_ARG;
-  for (int k = 0; k < 3; ++k) {
+  for (int k = 0; k < UA_KERNEL_KINDS; ++k) {
     ms[k] = 0.f;
     launches[k] = 0;
   }

@@ -64,6 +64,27 @@ cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cud
 // Log-sum-exp combine of split partials into bf16 output rows.
 cudaError_t launch_combine(const CombineParams& c, int head_dim, cudaStream_t stream);
 
+// Append-KV: new keys / values of a step into the paged cache.
+struct AppendParams {
+  const void* k_new;            // [total_tokens][Hkv][d] bf16
+  const void* v_new;
+  void* k_cache;                // [num_blocks][block_size][Hkv][d] bf16 or e4m3
+  void* v_cache;
+  const ua_tile* tiles;          // append tiles of the plan (one CTA each)
+  int32_t num_tiles;
+  const int32_t* block_tables;   // device [num_seqs][max_blocks_per_seq]
+  int32_t* err;                  // error word (UA_ERR_BOUNDS)
+  int64_t num_blocks;
+  int32_t row_elems;             // Hkv * d, a multiple of 8
+  int32_t max_blocks_per_seq;
+  int32_t block_size;
+  int32_t fp8;                   // 1: e4m3 cache
+  float k_scale;                 // e4m3 cache: code = e4m3(x / scale)
+  float v_scale;
+};
+
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
 // Test aid: copy the raw K/V rows each tile reads into dense buffers.
 cudaError_t launch_gather_debug(const KernelParams& p, const int64_t* row_offsets, int head_dim,
                                 int elt_bytes, void* k_out, void* v_out, cudaStream_t stream);

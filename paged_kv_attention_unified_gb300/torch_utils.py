@@ -10,7 +10,7 @@ from typing import Optional, Sequence
 
 import torch
 
-from . import (UA_KV_BF16, UA_KV_FP8_E4M3, Plan, ua_forward)
+from . import (UA_KV_BF16, UA_KV_FP8_E4M3, Plan, ua_append_kv, ua_forward)
 
 
 @dataclasses.dataclass
@@ -84,6 +84,13 @@ def forward(plan: Plan, b: DeviceBatch, out: Optional[torch.Tensor] = None,
                b.block_tables, b.num_blocks, b.max_q, b.max_kv, b.scale, b.k_scale, b.v_scale,
                stream=stream)
     return out
+
+
+def append_kv(plan: Plan, b: DeviceBatch, k_new: torch.Tensor, v_new: torch.Tensor,
+              stream=None) -> None:
+    """Write new K/V rows [total_q, Hkv, d] (bf16, device) into b's caches."""
+    ua_append_kv(plan.handle, k_new, v_new, b.k_cache, b.v_cache, b.block_tables, b.num_blocks,
+                 b.k_scale, b.v_scale, stream)
 
 
 def run(case, num_splits: int = 0, decode_rows_max: int = -1, device="cuda") -> torch.Tensor:

@@ -266,3 +266,9 @@ def test_prefill_list_ends_with_shortest_tiles(case):
             seen.add(key)
             prev = key
     assert info.num_prefill_ctas == min(152, len(pre))
+
+
+def test_append_rejects_a_null_plan_without_touching_cuda():
+    lib = ua.lib()
+    st = lib.ua_append_kv(None, 16, 16, 16, 16, 16, 1, 1.0, 1.0, None)
+    assert st == ua.UA_ERR_INVALID_ARG
