@@ -52,6 +52,7 @@ struct DecodeCfg {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // Key slot (0..15) of a step held as MMA row m of S^T. Chosen so that the
 // PV contraction slots 2t, 2t+1, 2t+8, 2t+9 of lane t are keys 4t..4t+3.
@@ -219,22 +220,32 @@ __device__ __forceinline__ void compute_step(WarpState<D>& st, const StepRegs<D,
     mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 8));
     mx[j] = fmaxf(mx[j], __shfl_xor_sync(0xffffffffu, mx[j], 16));
   }
-  float p[4];
+  // The reference max moves only when the row max grew by more than 2^8
+  // (log2 units 8): P and l use the same stale reference, so the result is
+  // exact up to rounding, P stays below 2^8, and the O rescale (a multiply of
+  // every accumulator) runs only on the rare steps where some row moved.
+  float p[4], alpha[2];
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const float m_new = fmaxf(st.m[j], mx[j]);
+    const bool grow = (st.m[j] == -INFINITY) || (m_new > st.m[j] + kRescaleThreshold);
+    const float m_use = grow ? m_new : st.m[j];
     // Rows with nothing visible yet keep m = -inf; subtract 0 instead so that
     // no -inf - -inf appears.
-    const float sub = (m_new == -INFINITY) ? 0.f : m_new;
-    const float alpha = ex2(st.m[j] - sub);
+    const float sub = (m_use == -INFINITY) ? 0.f : m_use;
+    alpha[j] = grow ? ex2(st.m[j] - sub) : 1.f;
     p[j] = ex2(x[j] - sub);
     p[j + 2] = ex2(x[j + 2] - sub);
-    st.l[j] = st.l[j] * alpha + p[j] + p[j + 2];
-    st.m[j] = m_new;
+    st.l[j] = st.l[j] * alpha[j] + p[j] + p[j + 2];
+    st.m[j] = m_use;
+  }
+  if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
     for (int c = 0; c < C::NC; ++c) {
-      st.acc[c][j] *= alpha;
-      st.acc[c][j + 2] *= alpha;
+      st.acc[c][0] *= alpha[0];
+      st.acc[c][2] *= alpha[0];
+      st.acc[c][1] *= alpha[1];
+      st.acc[c][3] *= alpha[1];
     }
   }
   // P^T as the B operand of the PV product: transpose the two 8x8 blocks.
