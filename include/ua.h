@@ -43,11 +43,12 @@
  *
  * Conventions.
  *  - The caller owns every tensor argument; the plan owns its device tile list,
- *    per-plan error word and split workspace, and frees them in
- *    ua_plan_destroy.
+ *    per-plan error word and split workspace (allocated stream-ordered from a
+ *    pool the library keeps per device), and frees them in ua_plan_destroy.
  *  - Device pointers must be 16-byte aligned and tensors contiguous.
  *  - All device work is ordered on the stream argument; nothing synchronises
- *    the host except ua_last_device_error and ua_plan_destroy.
+ *    the host except ua_last_device_error, ua_plan_kernel_times and
+ *    ua_forward_oneshot.
  *  - No entry point calls exit, abort or a device trap. Invalid arguments are
  *    rejected with a negative status before anything is launched.
  */
@@ -253,6 +254,9 @@ ua_status ua_plan_set_debug(ua_plan* plan, int32_t flags, int64_t wait_timeout_n
  * (UA_OK, UA_ERR_BOUNDS or UA_ERR_DEVICE_TIMEOUT) into *code and clears it. */
 ua_status ua_last_device_error(ua_plan* plan, int32_t* code);
 
+/* Frees the plan. Its device memory is released stream-ordered on the last
+ * stream the plan was used on (no host synchronisation): work already queued
+ * there may still use it, later work must not. */
 ua_status ua_plan_destroy(ua_plan* plan);
 
 /* Static string for a status code (never NULL). */

@@ -6,6 +6,7 @@
 #include <climits>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -46,6 +47,41 @@ namespace {
 
 ua_status from_cuda(cudaError_t e) { return e == cudaSuccess ? UA_OK : UA_ERR_CUDA; }
 
+// Plan memory comes from a stream-ordered pool the library owns (one per
+// device), which keeps up to kPoolKeepBytes of freed blocks for the next
+// plan: a serving loop that builds and drops a plan every step then never
+// calls the driver allocator, and destroying a plan does not wait for its
+// stream. The pool's own release threshold is a setting of this process only.
+constexpr uint64_t kPoolKeepBytes = 1ull << 30;
+constexpr int kMaxDevices = 64;
+
+cudaMemPool_t plan_pool(int device) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[kMaxDevices] = {};
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (pools[device] == nullptr) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = device;
+    cudaMemPool_t pool = nullptr;
+    if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) return nullptr;
+    uint64_t keep = kPoolKeepBytes;
+    cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    pools[device] = pool;
+  }
+  return pools[device];
+}
+
+cudaError_t plan_alloc(void** ptr, size_t bytes, int device, cudaStream_t stream) {
+  cudaMemPool_t pool = plan_pool(device);
+  if (pool == nullptr) return cudaErrorMemoryAllocation;
+  return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void free_plan_memory(ua_plan* p) {
@@ -56,8 +92,10 @@ void free_plan_memory(ua_plan* p) {
     }
   p->ev_pending.clear();
   p->ev_free.clear();
-  if (p->d_meta) cudaFree(p->d_meta);
-  if (p->d_ws) cudaFree(p->d_ws);
+  // stream-ordered: the memory returns to the pool once the plan's last
+  // stream has finished with it
+  if (p->d_meta) cudaFreeAsync(p->d_meta, p->last_stream);
+  if (p->d_ws) cudaFreeAsync(p->d_ws, p->last_stream);
   p->d_meta = nullptr;
   p->d_ws = nullptr;
 }
@@ -249,7 +287,9 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   if (n_grp) std::memcpy(host.data() + bytes_tiles, s.groups.data(), bytes_groups);
   if (n_app) std::memcpy(host.data() + off_app, s.append.data(), n_app * sizeof(ua_tile));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMalloc(&plan->d_meta, bytes_meta) != cudaSuccess) {
+  plan->last_stream = cs;
+  if (plan_alloc(&plan->d_meta, bytes_meta, plan->device, cs) != cudaSuccess) {
+    plan->d_meta = nullptr;
     free_plan_memory(plan);
     delete plan;
     return UA_ERR_CUDA;
@@ -263,7 +303,10 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   plan->d_prefill_counters = reinterpret_cast<int32_t*>(base + off_pc);
   plan->d_append = reinterpret_cast<ua_tile*>(base + off_app);
   if (plan->info.workspace_bytes > 0) {
-    if (cudaMalloc(&plan->d_ws, static_cast<size_t>(plan->info.workspace_bytes)) != cudaSuccess) {
+    if (plan_alloc(reinterpret_cast<void**>(&plan->d_ws),
+                   static_cast<size_t>(plan->info.workspace_bytes), plan->device,
+                   cs) != cudaSuccess) {
+      plan->d_ws = nullptr;
       free_plan_memory(plan);
       delete plan;
       return UA_ERR_CUDA;
@@ -303,7 +346,6 @@ ua_status ua_plan_destroy(ua_plan* plan) {
   int cur = 0;
   cudaGetDevice(&cur);
   if (cur != plan->device) cudaSetDevice(plan->device);
-  cudaStreamSynchronize(plan->last_stream);
   free_plan_memory(plan);
   if (cur != plan->device) cudaSetDevice(cur);
   delete plan;
