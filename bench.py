@@ -38,7 +38,10 @@ WORKLOAD_NAMES = {
        "32/8 heads, d128, bf16, bs16",
     4: "dense causal prefill: 4 seqs x 4096, 32/32 heads, d128, bf16, bs128, identity table",
     5: "long decode fp8: 8 seqs, kv 131072, 64/8 heads, d128, fp8 e4m3 KV, bs16",
+    6: "dense causal prefill over an fp8 cache: 4 seqs x 4096, 32/32 heads, d128, fp8 e4m3 KV, "
+       "bs16, random table (not a benchmark configuration: measures the fp8 prefill path)",
 }
+FLOP_CONFIGS = (4, 6)   # prefill-bound workloads, reported in TFLOP/s
 
 
 def algorithmic_work(case):
@@ -225,7 +228,7 @@ def _oracle_steps_worker(cfg, steps, step_budget_s):
 
 
 def _metric_for(cfg):
-    if cfg == 4:
+    if cfg in FLOP_CONFIGS:
         return "prefill TFLOP/s (algorithmic causal flops / step time)", "TFLOP/s"
     return "decode KV-read GB/s (algorithmic K/V+Q+O bytes / step time)", "GB/s"
 
@@ -236,7 +239,7 @@ def _dtype_for(case):
 
 
 def _rate(cfg, byts, flops, seconds):
-    return (flops / seconds / 1e12) if cfg == 4 else (byts / seconds / 1e9)
+    return (flops / seconds / 1e12) if cfg in FLOP_CONFIGS else (byts / seconds / 1e9)
 
 
 # ---- replicas across ranks (weak scaling: an independent batch per GPU) ----
@@ -345,7 +348,7 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, cores, sample = oracle_throughput(cfg, case, budget_s=args.cpu_budget)
-        if cfg == 4:
+        if cfg in FLOP_CONFIGS:
             v = v / max(byts, 1) * flops / 1e3  # GB/s -> TFLOP/s on the same sample mix
         cpu = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
 
@@ -399,7 +402,7 @@ def run_ours(args):
 
     # dominant kernel and its roofline, credited with the work of the sequences
     # the scheduler gave it (host-only schedule of the same batch)
-    kind = max(ktimes, key=lambda k: ktimes[k][0])
+    kind = max(("prefill", "decode"), key=lambda k: ktimes[k][0])
     kms, kn = ktimes[kind]
     avg_s = kms / 1e3 / max(kn, 1)
     _, pre_t, dec_t, _ = ua.ua_schedule(b.cu_host, b.kv_host, b.num_q_heads, b.num_kv_heads,
@@ -477,7 +480,7 @@ def run_ours(args):
                    "decode_tiles": info.num_decode_tiles, "prefill_tiles": info.num_prefill_tiles,
                    "split_tokens": info.split_tokens},
         "algorithmic": {"bytes_per_step": byts, "flops_per_step": flops},
-        "pct_of_peak": (value / world) / (tf_peak if cfg == 4 else hbm_peak),
+        "pct_of_peak": (value / world) / (tf_peak if cfg in FLOP_CONFIGS else hbm_peak),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
         "kernel_ms": {k: v[0] for k, v in ktimes.items()},
         "clocks": clk.summary(),

@@ -236,9 +236,10 @@ ua_status ua_plan_get_info(const ua_plan* plan, ua_plan_info* info);
  * ua_append_kv record a CUDA event pair on their stream around each kernel
  * launch (a few microseconds per launch); ua_plan_kernel_times synchronises,
  * sums the elapsed milliseconds and launch counts per kernel kind since the
- * last read -- index 0 prefill, 1 decode, 2 combine, 3 append -- into
- * ms[0..UA_KERNEL_KINDS-1] / launches[0..UA_KERNEL_KINDS-1], and clears them. */
-#define UA_KERNEL_KINDS 4
+ * last read -- index 0 prefill, 1 decode, 2 combine, 3 append, 4 fp8
+ * prefill staging -- into ms[0..UA_KERNEL_KINDS-1] /
+ * launches[0..UA_KERNEL_KINDS-1], and clears them. */
+#define UA_KERNEL_KINDS 5
 ua_status ua_plan_set_profiling(ua_plan* plan, int32_t enable);
 ua_status ua_plan_kernel_times(ua_plan* plan, float* ms, int64_t* launches);
 

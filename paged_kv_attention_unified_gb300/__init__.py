@@ -245,7 +245,7 @@ def ua_plan_set_debug(plan: int, flags: int, wait_timeout_ns: int = 0):
     _check(lib().ua_plan_set_debug(plan, int(flags), int(wait_timeout_ns)), "ua_plan_set_debug")
 
 
-KERNEL_KINDS = ("prefill", "decode", "combine", "append")
+KERNEL_KINDS = ("prefill", "decode", "combine", "append", "stage")
 
 
 def ua_plan_kernel_times(plan: int):

@@ -199,6 +199,41 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
                        return longer(a, b);
                      });
   }
+  // Staging pages for an fp8 cache: per sequence with prefill tiles, the
+  // logical pages of kStagePage keys from the lowest key any of its tiles
+  // reads to its last key.
+  if (p.prefill_staged && !s.prefill.empty()) {
+    std::vector<int64_t> lo(p.num_seqs, INT64_MAX);
+    for (const ua_tile& t : s.prefill) lo[t.seq] = std::min<int64_t>(lo[t.seq], t.kv_lo);
+    int32_t max_pages = 0;
+    for (int32_t q = 0; q < p.num_seqs; ++q)
+      if (lo[q] != INT64_MAX)
+        max_pages = std::max<int32_t>(max_pages,
+                                      static_cast<int32_t>(ceil_div(p.kv_lens[q], kStagePage)));
+    s.staged_max_blocks = max_pages;
+    s.staged_table.assign(static_cast<size_t>(p.num_seqs) * max_pages, -1);
+    int64_t next = 0;
+    for (int32_t q = 0; q < p.num_seqs; ++q) {
+      if (lo[q] == INT64_MAX) continue;
+      const int64_t pages = ceil_div(p.kv_lens[q], kStagePage);
+      for (int64_t i = lo[q] / kStagePage; i < pages; ++i) {
+        s.staged_table[static_cast<size_t>(q) * max_pages + i] = static_cast<int32_t>(next);
+        ua_tile t;
+        t.seq = q;
+        t.kv_head = 0;
+        t.row0 = static_cast<int32_t>(next);
+        t.nrows = static_cast<int32_t>(i);
+        t.kv_lo = static_cast<int32_t>(i * kStagePage);
+        t.kv_hi = static_cast<int32_t>(std::min<int64_t>(p.kv_lens[q], (i + 1) * kStagePage));
+        t.slot = -1;
+        t.group = -1;
+        s.stage.push_back(t);
+        ++next;
+      }
+    }
+    s.staged_pages = next;
+  }
+
   // 4. The persistent prefill CTAs take tiles in list order as they free up.
   // The bulk keeps the order above; the shortest tiles, up to
   // kPrefillTailShare of the work, move to the end, longest first, so that no

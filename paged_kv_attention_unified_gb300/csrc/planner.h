@@ -31,6 +31,7 @@ struct Problem {
   int32_t num_sms = 152;
   int32_t decode_rows_max = -1; // < 0: default
   bool prefill_ok = false;      // the prefill kernel can take this problem
+  bool prefill_staged = false;  // fp8 cache: the prefill kernel reads a bf16 staging copy
 };
 
 struct Schedule {
@@ -38,6 +39,16 @@ struct Schedule {
   std::vector<ua_tile> prefill;
   int32_t prefill_ctas = 0;  // persistent prefill CTAs: min(SMs, prefill tiles)
   std::vector<ua_tile> decode;
+  // fp8 caches: the keys and values the prefill tiles read are first widened
+  // to bf16 into a staging cache of kStagePage-slot pages (a sequence's pages
+  // consecutive), which the prefill kernel reads through staged_table
+  // [num_seqs][staged_max_blocks] (-1: no page). One stage tile per page:
+  // seq, row0 = staging page, nrows = logical page index, [kv_lo, kv_hi) =
+  // the keys it holds.
+  std::vector<int32_t> staged_table;
+  std::vector<ua_tile> stage;
+  int32_t staged_max_blocks = 0;
+  int64_t staged_pages = 0;
   // Append-KV tiles: up to kAppendTokens consecutive new tokens of one
   // sequence: seq, row0 = first token (row of k_new), nrows = tokens,
   // kv_lo = logical cache position of the first token, kv_hi = kv_lo + nrows.
@@ -65,6 +76,8 @@ constexpr int kDefaultDecodeRowsMax = 32;
 constexpr int kPrefillKeyTile = 128;
 // Rows of one tcgen05 query tile of the prefill kernel (two per prefill tile).
 constexpr int kPrefillQueryTile = 128;
+// Slots per page of the bf16 staging cache of fp8 prefills.
+constexpr int kStagePage = 128;
 // New tokens per append tile (one warp each in the append kernel).
 constexpr int kAppendTokens = 8;
 // Share of the prefill work (in 128 x 128 query-key blocks) kept for the end

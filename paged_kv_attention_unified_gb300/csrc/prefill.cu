@@ -607,7 +607,7 @@ __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const Softm
   // Epilogue: O / l -> bf16 row of the output. The next work tile's first PV
   // into this O is issued only after this warp's next P is ready, i.e. after
   // these loads have completed.
-  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const float inv = l > 0.f ? p.out_scale / l : 0.f;
   const bool row_ok = r < g.rows_t;
   const int tok = g.q_start + row / p.qpk;
   const int head = g.kv_head * p.qpk + row % p.qpk;

@@ -27,6 +27,10 @@ struct ua_plan {
   int32_t* d_counters = nullptr;   // per combine group, zero between calls
   int32_t* d_prefill_counters = nullptr;  // [2] persistent prefill tile queue, zero between calls
   ua_tile* d_append = nullptr;            // append-KV tiles
+  int32_t* d_staged_table = nullptr;      // fp8 prefill: staging page table
+  ua_tile* d_stage = nullptr;             // fp8 prefill: stage tiles
+  void* d_staged_k = nullptr;             // fp8 prefill: bf16 staging caches
+  void* d_staged_v = nullptr;
   float* d_ws = nullptr;           // split workspace: partial rows then lse values
   float* d_ws_o = nullptr;
   float* d_ws_lse = nullptr;
@@ -96,8 +100,12 @@ void free_plan_memory(ua_plan* p) {
   // stream has finished with it
   if (p->d_meta) cudaFreeAsync(p->d_meta, p->last_stream);
   if (p->d_ws) cudaFreeAsync(p->d_ws, p->last_stream);
+  if (p->d_staged_k) cudaFreeAsync(p->d_staged_k, p->last_stream);
+  if (p->d_staged_v) cudaFreeAsync(p->d_staged_v, p->last_stream);
   p->d_meta = nullptr;
   p->d_ws = nullptr;
+  p->d_staged_k = nullptr;
+  p->d_staged_v = nullptr;
 }
 
 ua::Problem make_problem(const int32_t* cu, const int32_t* kv, int32_t num_seqs, int32_t hq,
@@ -119,7 +127,12 @@ ua::Problem make_problem(const int32_t* cu, const int32_t* kv, int32_t num_seqs,
   p.num_splits = num_splits;
   p.num_sms = num_sms;
   p.decode_rows_max = decode_rows_max;
-  p.prefill_ok = hkv > 0 && hq % hkv == 0 && ua::prefill_supported(d, dtype, hq / hkv, bs);
+  // An fp8 cache's prefill runs on a bf16 staging copy of 128-slot pages.
+  const bool fp8 = dtype == UA_KV_FP8_E4M3;
+  p.prefill_ok = hkv > 0 && hq % hkv == 0 &&
+                 ua::prefill_supported(d, fp8 ? UA_KV_BF16 : dtype, hq / hkv,
+                                       fp8 ? ua::kStagePage : bs);
+  p.prefill_staged = fp8 && p.prefill_ok;
   return p;
 }
 
@@ -279,13 +292,18 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   const size_t off_pc = bytes_tiles + bytes_groups + 16 + n_grp * sizeof(int32_t);
   const size_t n_app = s.append.size();
   const size_t off_app = (off_pc + 2 * sizeof(int32_t) + 15) & ~static_cast<size_t>(15);
-  const size_t bytes_meta = off_app + n_app * sizeof(ua_tile);
+  const size_t n_stage = s.stage.size(), n_st = s.staged_table.size();
+  const size_t off_stage = off_app + n_app * sizeof(ua_tile);
+  const size_t off_st = off_stage + n_stage * sizeof(ua_tile);
+  const size_t bytes_meta = off_st + n_st * sizeof(int32_t);
   std::vector<uint8_t> host(bytes_meta, 0);
   if (n_pre) std::memcpy(host.data(), s.prefill.data(), n_pre * sizeof(ua_tile));
   if (n_dec) std::memcpy(host.data() + n_pre * sizeof(ua_tile), s.decode.data(),
                          n_dec * sizeof(ua_tile));
   if (n_grp) std::memcpy(host.data() + bytes_tiles, s.groups.data(), bytes_groups);
   if (n_app) std::memcpy(host.data() + off_app, s.append.data(), n_app * sizeof(ua_tile));
+  if (n_stage) std::memcpy(host.data() + off_stage, s.stage.data(), n_stage * sizeof(ua_tile));
+  if (n_st) std::memcpy(host.data() + off_st, s.staged_table.data(), n_st * sizeof(int32_t));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   plan->last_stream = cs;
   if (plan_alloc(&plan->d_meta, bytes_meta, plan->device, cs) != cudaSuccess) {
@@ -302,6 +320,18 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   plan->d_counters = reinterpret_cast<int32_t*>(base + bytes_tiles + bytes_groups + 16);
   plan->d_prefill_counters = reinterpret_cast<int32_t*>(base + off_pc);
   plan->d_append = reinterpret_cast<ua_tile*>(base + off_app);
+  plan->d_stage = reinterpret_cast<ua_tile*>(base + off_stage);
+  plan->d_staged_table = reinterpret_cast<int32_t*>(base + off_st);
+  if (s.staged_pages > 0) {
+    const size_t bytes = static_cast<size_t>(s.staged_pages) * ua::kStagePage *
+                         plan->prob.num_kv_heads * head_dim * 2;
+    if (plan_alloc(&plan->d_staged_k, bytes, plan->device, cs) != cudaSuccess ||
+        plan_alloc(&plan->d_staged_v, bytes, plan->device, cs) != cudaSuccess) {
+      free_plan_memory(plan);
+      delete plan;
+      return UA_ERR_CUDA;
+    }
+  }
   if (plan->info.workspace_bytes > 0) {
     if (plan_alloc(reinterpret_cast<void**>(&plan->d_ws),
                    static_cast<size_t>(plan->info.workspace_bytes), plan->device,
@@ -380,6 +410,31 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
   ua::KernelParams kp = base_params(plan, q, k_cache, v_cache, out, cu_query_lens, kv_lens,
                                     block_tables, num_blocks, scale, k_scale, v_scale);
   if (!s.prefill.empty()) {
+    const bool staged = plan->prob.prefill_staged;
+    const void* pk = k_cache;
+    const void* pv = v_cache;
+    if (staged) {
+      // fp8 cache: widen the prefill sequences' pages into the staging cache
+      ua::StageParams sp;
+      std::memset(&sp, 0, sizeof(sp));
+      sp.k_src = k_cache;
+      sp.v_src = v_cache;
+      sp.k_dst = plan->d_staged_k;
+      sp.v_dst = plan->d_staged_v;
+      sp.tiles = plan->d_stage;
+      sp.num_tiles = static_cast<int32_t>(s.stage.size());
+      sp.block_tables = block_tables;
+      sp.max_blocks_per_seq = plan->prob.max_blocks_per_seq;
+      sp.block_size = plan->prob.block_size;
+      sp.num_blocks = num_blocks;
+      sp.row_elems = plan->prob.num_kv_heads * plan->prob.head_dim;
+      sp.err = plan->d_err;
+      auto* sev = timing_begin(mp, 4, cs);
+      if (ua::launch_stage(sp, cs) != cudaSuccess) return UA_ERR_CUDA;
+      timing_end(sev, cs);
+      pk = plan->d_staged_k;
+      pv = plan->d_staged_v;
+    }
     ua::PrefillParams pp;
     std::memset(&pp, 0, sizeof(pp));
     pp.tiles = plan->d_prefill;
@@ -388,22 +443,23 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     pp.num_ctas = plan->info.num_prefill_ctas;
     pp.cu_query_lens = cu_query_lens;
     pp.kv_lens = kv_lens;
-    pp.block_tables = block_tables;
+    pp.block_tables = staged ? plan->d_staged_table : block_tables;
     pp.out = out;
     pp.err = plan->d_err;
-    pp.num_blocks = num_blocks;
-    pp.max_blocks_per_seq = plan->prob.max_blocks_per_seq;
-    pp.block_size = plan->prob.block_size;
+    pp.num_blocks = staged ? s.staged_pages : num_blocks;
+    pp.max_blocks_per_seq = staged ? s.staged_max_blocks : plan->prob.max_blocks_per_seq;
+    pp.block_size = staged ? ua::kStagePage : plan->prob.block_size;
     pp.num_q_heads = plan->prob.num_q_heads;
     pp.qpk = kp.qpk;
     pp.causal = plan->prob.causal;
     pp.window = plan->prob.window;
     pp.score_scale_log2 = kp.score_scale_log2;
-    pp.rows_per_box = plan->prob.block_size < 128 ? plan->prob.block_size : 128;
+    pp.out_scale = kp.v_scale;
+    pp.rows_per_box = pp.block_size < 128 ? pp.block_size : 128;
     pp.timeout_ns = plan->wait_timeout_ns;
     pp.debug_flags = plan->debug_flags;
     auto* ev = timing_begin(mp, 0, cs);
-    if (ua::launch_prefill(pp, q, k_cache, v_cache, plan->total_q, plan->prob.head_dim,
+    if (ua::launch_prefill(pp, q, pk, pv, plan->total_q, plan->prob.head_dim,
                            plan->prob.num_kv_heads, cs) != cudaSuccess)
       return UA_ERR_CUDA;
     timing_end(ev, cs);

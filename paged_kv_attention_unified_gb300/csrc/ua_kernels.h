@@ -25,7 +25,8 @@ struct PrefillParams {
   int32_t qpk;
   int32_t causal;
   int32_t window;
-  float score_scale_log2;   // scale * log2(e)
+  float score_scale_log2;   // scale * log2(e) (* k_scale for a staged fp8 cache)
+  float out_scale;          // multiplies O / l (v_scale for a staged fp8 cache, else 1)
   int32_t rows_per_box;     // keys per TMA box: min(block_size, 128)
   uint64_t timeout_ns;      // bound of every mbarrier wait
   int32_t debug_flags;      // bit 0: the producer issues nothing (timeout test)
@@ -84,6 +85,25 @@ struct AppendParams {
 };
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+
+// fp8 prefill staging: e4m3 pages of the prefill sequences -> bf16 staging
+// pages of 128 slots (exact, scale-free).
+struct StageParams {
+  const void* k_src;             // e4m3 caches [num_blocks][block_size][Hkv][d]
+  const void* v_src;
+  void* k_dst;                   // bf16 staging [pages][128][Hkv][d]
+  void* v_dst;
+  const ua_tile* tiles;          // stage tiles of the plan (one CTA each)
+  int32_t num_tiles;
+  const int32_t* block_tables;   // device [num_seqs][max_blocks_per_seq]
+  int32_t max_blocks_per_seq;
+  int32_t block_size;
+  int64_t num_blocks;
+  int32_t row_elems;             // Hkv * d, a multiple of 8
+  int32_t* err;                  // error word (UA_ERR_BOUNDS)
+};
+
+cudaError_t launch_stage(const StageParams& p, cudaStream_t stream);
 
 // Test aid: copy the raw K/V rows each tile reads into dense buffers.
 cudaError_t launch_gather_debug(const KernelParams& p, const int64_t* row_offsets, int head_dim,

@@ -160,3 +160,53 @@ def test_bounded_wait_reports_timeout_and_context_survives():
         torch.cuda.synchronize()
         assert plan.last_device_error() == 0
     assert_close(as_f64(out), oracle_full(case), W.BF16, "after timeout")
+
+
+# ---- prefill over an fp8 (e4m3) cache: staged to bf16, then the tcgen05 kernel
+
+def _check_fp8(case, decode_rows_max=0):
+    b = tu.to_device(case)
+    with tu.make_plan(b, decode_rows_max=decode_rows_max) as plan:
+        assert plan.info.num_prefill_tiles > 0
+        out = tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    return assert_close(as_f64(out), oracle_full(case), case.kv_dtype, case.name)
+
+
+@pytest.mark.parametrize("qpk,hkv,d,bs", [(4, 2, 128, 16), (1, 4, 64, 32), (8, 1, 128, 64),
+                                          (2, 2, 128, 128), (1, 2, 64, 256)])
+def test_fp8_prefill_matches_oracle(qpk, hkv, d, bs):
+    _check_fp8(W.make_case(f"fp8p_{qpk}_{bs}", [300, 77, 150], [300, 500, 460], qpk * hkv, hkv,
+                           d, bs, kv_dtype=W.FP8, seed=400 + bs))
+
+
+def test_fp8_prefill_window_noncausal_and_poison():
+    _check_fp8(W.make_case("fp8p_win", [400, 260], [900, 260], 8, 2, 128, 16, window=150,
+                           kv_dtype=W.FP8, seed=410))
+    _check_fp8(W.make_case("fp8p_nc", [200, 90], [600, 90], 8, 2, 128, 16, causal=False,
+                           kv_dtype=W.FP8, seed=411))
+    _check_fp8(W.make_case("fp8p_poison", [333, 150], [700, 181], 8, 2, 128, 16, poison=True,
+                           kv_dtype=W.FP8, seed=412))
+
+
+def test_fp8_mixed_batch_prefill_and_decode():
+    """Long sequences through the staged prefill, single tokens through the fp8
+    decode kernel, in one plan."""
+    case = W.make_case("fp8_mixed", [1, 600, 1, 1, 37, 900], [3000, 1400, 70, 5000, 37, 900], 16,
+                       4, 128, 16, kv_dtype=W.FP8, seed=420)
+    _check_fp8(case, decode_rows_max=32)
+
+
+def test_full_size_fp8_dense_prefill_sampled():
+    case = W.config6_dense_prefill_fp8()
+    b = tu.to_device(case)
+    with tu.make_plan(b) as plan:
+        assert plan.info.num_decode_tiles == 0
+        out = tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    rows = sample_rows(case, 24, seed=6)
+    exp = oracle_rows(case, rows)
+    got = np.stack([as_f64(out[t, h]) for t, h in rows])
+    assert_close(got, exp, case.kv_dtype, case.name)

@@ -263,12 +263,21 @@ def config5_long_fp8_decode(seed: int = 0, poison: bool = False) -> Case:
                      kv_dtype=FP8, seed=seed, poison=poison)
 
 
+def config6_dense_prefill_fp8(seed: int = 0, poison: bool = False) -> Case:
+    """Config 4's prefill over a paged fp8 e4m3 cache: batch 4, 32 heads (MHA),
+    q = kv = 4096, d 128, block_size 16, random table (not one of the five
+    benchmark configurations: it measures the fp8 prefill path)."""
+    return make_case("dense_causal_prefill_fp8_b4_h32_l4096_d128_bs16", [4096] * 4, [4096] * 4,
+                     32, 32, 128, 16, kv_dtype=FP8, seed=seed, poison=poison)
+
+
 CONFIGS = {
     1: config1_tiny_mixed,
     2: config2_pure_decode,
     3: config3_mixed,
     4: config4_dense_prefill,
     5: config5_long_fp8_decode,
+    6: config6_dense_prefill_fp8,
 }
 
 
