@@ -617,8 +617,8 @@ cudaError_t launch_decode_d(const KernelParams& p, cudaStream_t stream) {
     e = encode_kv_page_map(&mv, p.v_cache, elt, D, p.num_kv_heads, p.block_size, p.num_blocks,
                            PL::kBoxDims, 16, PL::kSwizzle);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Ring<D, FP8>::kAlloc);
+  static std::atomic<uint64_t> smem_set{0};
+  e = set_smem_once(decode_kernel<D, FP8>, Ring<D, FP8>::kAlloc, smem_set);
   if (e != cudaSuccess) return e;
   decode_kernel<D, FP8><<<p.num_tiles, kThreads, Ring<D, FP8>::kAlloc, stream>>>(mk, mv, p);
   return cudaGetLastError();

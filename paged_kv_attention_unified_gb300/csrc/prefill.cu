@@ -760,9 +760,8 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
     checked = 1;
   }
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Smem<D>::kAlloc);
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e = set_smem_once(prefill_kernel<D>, Smem<D>::kAlloc, smem_set);
   if (e != cudaSuccess) return e;
   prefill_kernel<D><<<p.num_ctas, kThreads, Smem<D>::kAlloc, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();

@@ -86,6 +86,47 @@ cudaError_t plan_alloc(void** ptr, size_t bytes, int device, cudaStream_t stream
   return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
 }
 
+// Pinned host blocks for the plan's tile-list upload. A copy from pageable
+// memory first waits for everything queued on its stream (for a step that
+// has just queued the H2D copy of its inputs, that is the whole copy); from
+// pinned memory it is queued like a kernel, so scheduling the next plan
+// overlaps the input copy. A block is reused once the event recorded after
+// its copy has completed; blocks are kept for the life of the process.
+struct PinnedBlock {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  cudaEvent_t done = nullptr;
+};
+
+std::mutex g_pinned_mu;
+std::vector<PinnedBlock> g_pinned_free;
+
+bool pinned_take(size_t bytes, PinnedBlock* out) {
+  std::lock_guard<std::mutex> lock(g_pinned_mu);
+  for (size_t i = 0; i < g_pinned_free.size(); ++i) {
+    PinnedBlock& b = g_pinned_free[i];
+    if (b.bytes >= bytes && cudaEventQuery(b.done) == cudaSuccess) {
+      *out = b;
+      g_pinned_free.erase(g_pinned_free.begin() + static_cast<std::ptrdiff_t>(i));
+      return true;
+    }
+  }
+  PinnedBlock b;
+  b.bytes = bytes < (64u << 10) ? (64u << 10) : bytes;
+  if (cudaMallocHost(&b.ptr, b.bytes) != cudaSuccess) return false;
+  if (cudaEventCreateWithFlags(&b.done, cudaEventDisableTiming) != cudaSuccess) {
+    cudaFreeHost(b.ptr);
+    return false;
+  }
+  *out = b;
+  return true;
+}
+
+void pinned_give_back(const PinnedBlock& b) {
+  std::lock_guard<std::mutex> lock(g_pinned_mu);
+  g_pinned_free.push_back(b);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void free_plan_memory(ua_plan* p) {
@@ -296,18 +337,25 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   const size_t off_stage = off_app + n_app * sizeof(ua_tile);
   const size_t off_st = off_stage + n_stage * sizeof(ua_tile);
   const size_t bytes_meta = off_st + n_st * sizeof(int32_t);
-  std::vector<uint8_t> host(bytes_meta, 0);
-  if (n_pre) std::memcpy(host.data(), s.prefill.data(), n_pre * sizeof(ua_tile));
-  if (n_dec) std::memcpy(host.data() + n_pre * sizeof(ua_tile), s.decode.data(),
+  PinnedBlock staging;
+  if (!pinned_take(bytes_meta, &staging)) {
+    delete plan;
+    return UA_ERR_CUDA;
+  }
+  uint8_t* host = static_cast<uint8_t*>(staging.ptr);
+  std::memset(host, 0, bytes_meta);
+  if (n_pre) std::memcpy(host, s.prefill.data(), n_pre * sizeof(ua_tile));
+  if (n_dec) std::memcpy(host + n_pre * sizeof(ua_tile), s.decode.data(),
                          n_dec * sizeof(ua_tile));
-  if (n_grp) std::memcpy(host.data() + bytes_tiles, s.groups.data(), bytes_groups);
-  if (n_app) std::memcpy(host.data() + off_app, s.append.data(), n_app * sizeof(ua_tile));
-  if (n_stage) std::memcpy(host.data() + off_stage, s.stage.data(), n_stage * sizeof(ua_tile));
-  if (n_st) std::memcpy(host.data() + off_st, s.staged_table.data(), n_st * sizeof(int32_t));
+  if (n_grp) std::memcpy(host + bytes_tiles, s.groups.data(), bytes_groups);
+  if (n_app) std::memcpy(host + off_app, s.append.data(), n_app * sizeof(ua_tile));
+  if (n_stage) std::memcpy(host + off_stage, s.stage.data(), n_stage * sizeof(ua_tile));
+  if (n_st) std::memcpy(host + off_st, s.staged_table.data(), n_st * sizeof(int32_t));
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   plan->last_stream = cs;
   if (plan_alloc(&plan->d_meta, bytes_meta, plan->device, cs) != cudaSuccess) {
     plan->d_meta = nullptr;
+    pinned_give_back(staging);
     free_plan_memory(plan);
     delete plan;
     return UA_ERR_CUDA;
@@ -327,6 +375,7 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
                          plan->prob.num_kv_heads * head_dim * 2;
     if (plan_alloc(&plan->d_staged_k, bytes, plan->device, cs) != cudaSuccess ||
         plan_alloc(&plan->d_staged_v, bytes, plan->device, cs) != cudaSuccess) {
+      pinned_give_back(staging);
       free_plan_memory(plan);
       delete plan;
       return UA_ERR_CUDA;
@@ -337,6 +386,7 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
                    static_cast<size_t>(plan->info.workspace_bytes), plan->device,
                    cs) != cudaSuccess) {
       plan->d_ws = nullptr;
+      pinned_give_back(staging);
       free_plan_memory(plan);
       delete plan;
       return UA_ERR_CUDA;
@@ -344,8 +394,12 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
     plan->d_ws_o = static_cast<float*>(plan->d_ws);
     plan->d_ws_lse = plan->d_ws_o + s.num_slots * UA_DECODE_ROWS * static_cast<int64_t>(head_dim);
   }
-  if (cudaMemcpyAsync(plan->d_meta, host.data(), bytes_meta, cudaMemcpyHostToDevice, cs) !=
-      cudaSuccess) {
+  const bool copied =
+      cudaMemcpyAsync(plan->d_meta, host, bytes_meta, cudaMemcpyHostToDevice, cs) == cudaSuccess;
+  // the block returns to the pool; it is reused only after this event
+  cudaEventRecord(staging.done, cs);
+  pinned_give_back(staging);
+  if (!copied) {
     free_plan_memory(plan);
     delete plan;
     return UA_ERR_CUDA;

@@ -1,12 +1,30 @@
 // Launch entry points of the device kernels (host side of each .cu file).
 #pragma once
 
+#include <atomic>
+#include <cstdint>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "ua_device.cuh"
 
 namespace ua {
+
+// Sets a kernel's dynamic shared-memory limit once per device (the driver
+// keeps it for the life of the context). `done` is a per-kernel bitmask of
+// devices; devices beyond 63 are set on every call.
+template <typename Kernel>
+cudaError_t set_smem_once(Kernel kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 struct PrefillParams {
   const ua_tile* tiles;       // taken in list order by the persistent CTAs
