@@ -52,12 +52,15 @@ __global__ void __launch_bounds__(32 * UA_DECODE_ROWS) combine_kernel(const Comb
     const float w = wts[n][s];
     if (w == 0.f) continue;
     const float* src = base + static_cast<int64_t>(s) * UA_DECODE_ROWS * D;
-    if constexpr (kPer == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] += w * v.x;
-      acc[1] += w * v.y;
-      acc[2] += w * v.z;
-      acc[3] += w * v.w;
+    if constexpr (kPer % 4 == 0) {
+#pragma unroll
+      for (int e = 0; e < kPer; e += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src + e);
+        acc[e] += w * v.x;
+        acc[e + 1] += w * v.y;
+        acc[e + 2] += w * v.z;
+        acc[e + 3] += w * v.w;
+      }
     } else {
       const float2 v = *reinterpret_cast<const float2*>(src);
       acc[0] += w * v.x;
@@ -69,9 +72,12 @@ __global__ void __launch_bounds__(32 * UA_DECODE_ROWS) combine_kernel(const Comb
   const int head = grp.kv_head * c.qpk + r % c.qpk;
   uint8_t* dst = reinterpret_cast<uint8_t*>(c.out) +
                  ((static_cast<int64_t>(tok) * c.num_q_heads + head) * D + lane * kPer) * 2;
-  if constexpr (kPer == 4) {
-    *reinterpret_cast<uint2*>(dst) =
-        make_uint2(pack2<false>(acc[0] * inv, acc[1] * inv), pack2<false>(acc[2] * inv, acc[3] * inv));
+  if constexpr (kPer % 4 == 0) {
+#pragma unroll
+    for (int e = 0; e < kPer; e += 4)
+      *reinterpret_cast<uint2*>(dst + 2 * e) =
+          make_uint2(pack2<false>(acc[e] * inv, acc[e + 1] * inv),
+                     pack2<false>(acc[e + 2] * inv, acc[e + 3] * inv));
   } else {
     *reinterpret_cast<uint32_t*>(dst) = pack2<false>(acc[0] * inv, acc[1] * inv);
   }
@@ -107,7 +113,9 @@ __global__ void gather_debug_kernel(const KernelParams p, const int64_t* row_off
 
 cudaError_t launch_combine(const CombineParams& c, int head_dim, cudaStream_t stream) {
   if (c.num_groups <= 0) return cudaSuccess;
-  if (head_dim == 128)
+  if (head_dim == 256)
+    combine_kernel<256><<<c.num_groups, 32 * UA_DECODE_ROWS, 0, stream>>>(c);
+  else if (head_dim == 128)
     combine_kernel<128><<<c.num_groups, 32 * UA_DECODE_ROWS, 0, stream>>>(c);
   else
     combine_kernel<64><<<c.num_groups, 32 * UA_DECODE_ROWS, 0, stream>>>(c);

@@ -112,8 +112,8 @@ struct StepRegs {
 // step's K and V rows (16 rows of head_dim elements, as the TMA box lands).
 // Keys at or beyond kv_hi read as zero (the page may hold anything there).
 template <int D, bool FP8>
-__device__ __forceinline__ void read_step(StepRegs<D, FP8>& r, const uint8_t* kp,
-                                          const uint8_t* vp, int base, int kv_hi, int g, int t) {
+__device__ __forceinline__ void read_k(StepRegs<D, FP8>& r, const uint8_t* kp, int base,
+                                       int kv_hi, int g, int t) {
   using C = DecodeCfg<D, FP8>;
   using PL = PageLayout<D, FP8>;
 #pragma unroll
@@ -131,6 +131,13 @@ __device__ __forceinline__ void read_step(StepRegs<D, FP8>& r, const uint8_t* kp
       r.k[h][4 * l + 3] = x.w;
     }
   }
+}
+
+template <int D, bool FP8>
+__device__ __forceinline__ void read_v(StepRegs<D, FP8>& r, const uint8_t* vp, int base,
+                                       int kv_hi, int g, int t) {
+  using C = DecodeCfg<D, FP8>;
+  using PL = PageLayout<D, FP8>;
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const int key = 4 * t + j;
@@ -155,6 +162,11 @@ __device__ __forceinline__ void read_step(StepRegs<D, FP8>& r, const uint8_t* kp
   }
 }
 
+// Head dims above 128 read V only after the softmax, so that the K and V
+// fragments of a step are never live together (register budget).
+template <int D>
+constexpr bool kLateV = D > 128;
+
 // Per-warp online-softmax state for the two rows (columns n = 2t, 2t+1) a lane
 // holds, plus its O^T accumulator fragments.
 template <int D>
@@ -174,7 +186,8 @@ struct StepMask {
 };
 
 template <int D, bool FP8>
-__device__ __forceinline__ void compute_step(WarpState<D>& st, const StepRegs<D, FP8>& r,
+__device__ __forceinline__ void compute_step(WarpState<D>& st, StepRegs<D, FP8>& r,
+                                             const uint8_t* vp, int kv_hi,
                                              const uint32_t (&qb)[D / 16][2], const float (&cc)[2],
                                              const StepMask& mk, int base, int g, int t) {
   using C = DecodeCfg<D, FP8>;
@@ -248,6 +261,7 @@ __device__ __forceinline__ void compute_step(WarpState<D>& st, const StepRegs<D,
       st.acc[c][3] *= alpha[1];
     }
   }
+  if constexpr (kLateV<D>) read_v<D, FP8>(r, vp, base, kv_hi, g, t);
   // P^T as the B operand of the PV product: transpose the two 8x8 blocks.
   const uint32_t pb0 = movmatrix_trans(pack2<FP8>(p[0], p[1]));
   const uint32_t pb1 = movmatrix_trans(pack2<FP8>(p[2], p[3]));
@@ -290,7 +304,7 @@ struct Ring {
 };
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
     decode_kernel(const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const KernelParams p) {
   using C = DecodeCfg<D, FP8>;
@@ -467,8 +481,10 @@ __global__ void __launch_bounds__(kThreads, 3)
         break;
       }
       const uint8_t* stage = ring + st * RC::kStage;
-      read_step<D, FP8>(r, stage, stage + 16 * RC::kRowBytes, step_base(done), kv_hi, g, t);
-      compute_step<D, FP8>(st_state, r, qb, cc, mk, step_base(done), g, t);
+      const uint8_t* vstage = stage + 16 * RC::kRowBytes;
+      read_k<D, FP8>(r, stage, step_base(done), kv_hi, g, t);
+      if constexpr (!kLateV<D>) read_v<D, FP8>(r, vstage, step_base(done), kv_hi, g, t);
+      compute_step<D, FP8>(st_state, r, vstage, kv_hi, qb, cc, mk, step_base(done), g, t);
       __syncwarp();  // every lane has consumed the stage: it may be refilled
       if (issued < my_n) {
         if ((issued & 31) == 0) refill_ids(issued >> 5);
@@ -539,8 +555,11 @@ __global__ void __launch_bounds__(kThreads, 3)
       packed[e] = pack2<false>(vals[2 * e] * mult, vals[2 * e + 1] * mult);
     uint8_t* dst = reinterpret_cast<uint8_t*>(p.out) +
                    ((static_cast<int64_t>(tok) * p.num_q_heads + head) * D + d0) * 2;
-    if constexpr (kSeg == 8) {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+    if constexpr (kSeg % 8 == 0) {
+#pragma unroll
+      for (int i = 0; i < kSeg / 8; ++i)
+        *reinterpret_cast<uint4*>(dst + 16 * i) =
+            make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
     } else {
       *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
     }
@@ -628,9 +647,12 @@ cudaError_t launch_decode_d(const KernelParams& p, cudaStream_t stream) {
 
 cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cudaStream_t stream) {
   if (p.num_tiles <= 0) return cudaSuccess;
-  if (kv_dtype == UA_KV_BF16)
+  if (kv_dtype == UA_KV_BF16) {
+    if (head_dim == 256) return launch_decode_d<256, false>(p, stream);
     return head_dim == 128 ? launch_decode_d<128, false>(p, stream)
                            : launch_decode_d<64, false>(p, stream);
+  }
+  if (head_dim == 256) return launch_decode_d<256, true>(p, stream);
   return head_dim == 128 ? launch_decode_d<128, true>(p, stream)
                          : launch_decode_d<64, true>(p, stream);
 }

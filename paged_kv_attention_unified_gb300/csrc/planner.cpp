@@ -43,7 +43,7 @@ ua_status validate(const Problem& p) {
   if (p.causal != 0 && p.causal != 1) return UA_ERR_INVALID_ARG;
   if (p.num_seqs > 0 && (p.cu_query_lens == nullptr || p.kv_lens == nullptr))
     return UA_ERR_INVALID_ARG;
-  if (p.head_dim != 64 && p.head_dim != 128) return UA_ERR_UNSUPPORTED;
+  if (p.head_dim != 64 && p.head_dim != 128 && p.head_dim != 256) return UA_ERR_UNSUPPORTED;
   if (p.block_size % kKeyStep != 0) return UA_ERR_UNSUPPORTED;
   if (p.num_seqs == 0) return UA_OK;
   if (p.cu_query_lens[0] != 0) return UA_ERR_INVALID_ARG;

@@ -63,7 +63,7 @@ def test_invalid_problems_are_rejected(bad):
     assert e.value.status == ua.UA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("d,bs", [(96, 16), (128, 8), (256, 16), (64, 24)])
+@pytest.mark.parametrize("d,bs", [(96, 16), (128, 8), (512, 16), (32, 16), (64, 24)])
 def test_unsupported_shapes(d, bs):
     with pytest.raises(ua.UAError) as e:
         ua.ua_schedule([0, 1], [5], 4, 4, d, bs, 64)
@@ -272,3 +272,12 @@ def test_append_rejects_a_null_plan_without_touching_cuda():
     lib = ua.lib()
     st = lib.ua_append_kv(None, 16, 16, 16, 16, 16, 1, 1.0, 1.0, None)
     assert st == ua.UA_ERR_INVALID_ARG
+
+
+def test_head_dim_256_is_decode_only():
+    """head_dim 256 runs in the decode kernel (the prefill kernel takes 64 and
+    128): every row, long prefills included, lands in decode tiles."""
+    info, pre, dec, grp = ua.ua_schedule([0, 1, 301], [500, 800], 8, 2, 256, 16, 64)
+    assert info.num_prefill_tiles == 0 and info.num_decode_tiles > 0
+    rows = {(t["seq"], t["kv_head"], r) for t in dec for r in range(t["row0"], t["row0"] + t["nrows"])}
+    assert len(rows) == 301 * 4 * 2

@@ -192,3 +192,37 @@ def test_full_size_decode_configs_sampled(cfg):
     g = np.stack([as_f64(got[t, h]) for t, h in rows])
     assert_close(g, exp, case.kv_dtype, case.name)
     assert torch.isfinite(got.float()).all()
+
+
+# ---- head_dim 256 (decode kernel only: V fragments read after the softmax)
+
+@pytest.mark.parametrize("dtype", [W.BF16, W.FP8])
+def test_head_dim_256_random(dtype):
+    for seed in (600, 601):
+        _check(W.random_small_case(seed, kv_dtype=dtype, head_dim=256, num_q_heads=8,
+                                   num_kv_heads=2, max_kv=900))
+
+
+def test_head_dim_256_splits_window_and_long_prefill():
+    case = W.make_case("d256_mix", [1, 1, 130], [3000, 70, 400], 16, 4, 256, 16, seed=610)
+    _check(case, num_splits=7)
+    _check(W.make_case("d256_win", [1, 50], [2000, 600], 8, 2, 256, 32, window=300, seed=611))
+    _check(W.make_case("d256_fp8", [1, 3], [5000, 900], 16, 2, 256, 16, kv_dtype=W.FP8,
+                       seed=612), num_splits=16)
+
+
+def test_head_dim_256_allocation_free_entry_point_matches_oracle():
+    # a decode batch: the entry point's fixed scratch sizes split pieces for
+    # every row tile of the longest query
+    case = W.make_case("d256_static", [1, 1, 1, 1], [3000, 70, 1200, 16], 8, 2, 256, 16, seed=620)
+    b = tu.to_device(case)
+    out = b.new_out()
+    err = torch.full((1,), -99, dtype=torch.int32, device="cuda")
+    ua.ua_forward_static_scratch(
+        b.q, b.k_cache, b.v_cache, out, b.cu_query_lens, b.kv_lens, b.block_tables,
+        b.num_q_heads, b.num_kv_heads, b.head_dim, b.block_size, int(b.block_tables.shape[1]),
+        b.num_blocks, b.kv_dtype, b.max_q, b.max_kv, b.scale, causal=b.causal, window=b.window,
+        k_scale=b.k_scale, v_scale=b.v_scale, num_splits=4, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(as_f64(out), oracle_full(case), case.kv_dtype, case.name)

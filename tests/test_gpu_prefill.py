@@ -210,3 +210,30 @@ def test_full_size_fp8_dense_prefill_sampled():
     exp = oracle_rows(case, rows)
     got = np.stack([as_f64(out[t, h]) for t, h in rows])
     assert_close(got, exp, case.kv_dtype, case.name)
+
+
+def test_many_ragged_sequences_through_both_kernels():
+    """400 sequences: single tokens, short and long prefills with and without
+    prior context, one plan, both kernels, the prefill tile queue busy."""
+    rng = np.random.default_rng(500)
+    ql, kv = [], []
+    for i in range(400):
+        kind = i % 4
+        q = 1 if kind == 0 else int(rng.integers(2, 40)) if kind == 1 else \
+            int(rng.integers(40, 400)) if kind == 2 else int(rng.integers(400, 1200))
+        ql.append(q)
+        kv.append(q + int(rng.integers(0, 600)))
+    case = W.make_case("many_seqs", ql, kv, 16, 4, 128, 16, seed=501)
+    b = tu.to_device(case)
+    with tu.make_plan(b) as plan:
+        info = plan.info
+        assert info.num_prefill_tiles > 152 and info.num_decode_tiles > 0
+        out = tu.forward(plan, b)
+        out2 = tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    rows = sample_rows(case, 64, seed=502)
+    exp = oracle_rows(case, rows)
+    got = np.stack([as_f64(out[t, h]) for t, h in rows])
+    assert_close(got, exp, case.kv_dtype, case.name)
