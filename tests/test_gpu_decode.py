@@ -226,3 +226,28 @@ def test_head_dim_256_allocation_free_entry_point_matches_oracle():
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_close(as_f64(out), oracle_full(case), case.kv_dtype, case.name)
+
+
+def test_plan_churn_reuses_pooled_memory():
+    """A serving loop builds and drops a plan every step: plan memory comes
+    from the library's stream-ordered pool and pinned upload blocks, so 200
+    more steps leave device memory use where it was, and the results stay
+    right."""
+    case = W.config1_tiny_mixed()
+    b = tu.to_device(case)
+    exp = oracle_full(case)
+
+    def step():
+        with tu.make_plan(b, num_splits=3) as plan:
+            return tu.forward(plan, b)
+
+    for _ in range(20):
+        step()
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(200):
+        out = step()
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert abs(free1 - free0) < 64 * 2 ** 20, (free0, free1)
+    assert_close(as_f64(out), exp, case.kv_dtype, case.name)
