@@ -175,9 +175,13 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
  * UA_ERR_BOUNDS is recorded in the plan's error word.
  * max_q / max_kv: the largest q_len / kv_len (checked against the plan).
  * scale: multiplies q.k as given (not assumed to be 1/sqrt(d)).
- * Launches the prefill kernel, the decode kernel and, if any tile was split,
- * the combine kernel on `stream`. Not thread-safe per plan: calls that share
- * a plan must be ordered (they share its split workspace).
+ * Launches the prefill kernel (after the staging kernel for an fp8 cache)
+ * and the decode kernel (which merges split pieces itself) in the order of
+ * `stream`: when the batch has both, the decode kernel runs on a side stream
+ * of the library's pool that starts after everything queued on `stream` and
+ * that `stream` waits for, so that the two kernels share the GPU; work queued
+ * on `stream` afterwards sees the whole result. Not thread-safe per plan:
+ * calls that share a plan must be ordered (they share its split workspace).
  */
 ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
                      const void* v_cache, void* out, const int32_t* cu_query_lens,

@@ -31,6 +31,11 @@ struct ua_plan {
   ua_tile* d_stage = nullptr;             // fp8 prefill: stage tiles
   void* d_staged_k = nullptr;             // fp8 prefill: bf16 staging caches
   void* d_staged_v = nullptr;
+  // A batch with both prefill and decode tiles runs the two kernels on two
+  // streams (the caller's and a side stream from the library's pool), forked
+  // and joined with events, so that each fills the SMs the other leaves.
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   float* d_ws = nullptr;           // split workspace: partial rows then lse values
   float* d_ws_o = nullptr;
   float* d_ws_lse = nullptr;
@@ -127,6 +132,33 @@ void pinned_give_back(const PinnedBlock& b) {
   g_pinned_free.push_back(b);
 }
 
+// Side streams for the decode half of a mixed forward, reused across plans
+// (creating a stream per plan would cost every mixed serving step): a plan
+// takes one on its first mixed forward and returns it when destroyed; work
+// still queued on it is unaffected (the next user queues behind it).
+std::mutex g_side_mu;
+std::vector<std::pair<int, cudaStream_t>> g_side_free;
+
+cudaStream_t side_take(int device) {
+  {
+    std::lock_guard<std::mutex> lock(g_side_mu);
+    for (size_t i = 0; i < g_side_free.size(); ++i)
+      if (g_side_free[i].first == device) {
+        cudaStream_t st = g_side_free[i].second;
+        g_side_free.erase(g_side_free.begin() + static_cast<std::ptrdiff_t>(i));
+        return st;
+      }
+  }
+  cudaStream_t st = nullptr;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+  return st;
+}
+
+void side_give_back(int device, cudaStream_t st) {
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  g_side_free.emplace_back(device, st);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void free_plan_memory(ua_plan* p) {
@@ -139,6 +171,11 @@ void free_plan_memory(ua_plan* p) {
   p->ev_free.clear();
   // stream-ordered: the memory returns to the pool once the plan's last
   // stream has finished with it
+  if (p->side) side_give_back(p->device, p->side);
+  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+  if (p->ev_join) cudaEventDestroy(p->ev_join);
+  p->side = nullptr;
+  p->ev_fork = p->ev_join = nullptr;
   if (p->d_meta) cudaFreeAsync(p->d_meta, p->last_stream);
   if (p->d_ws) cudaFreeAsync(p->d_ws, p->last_stream);
   if (p->d_staged_k) cudaFreeAsync(p->d_staged_k, p->last_stream);
@@ -463,7 +500,7 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
   mp->last_stream = cs;
   ua::KernelParams kp = base_params(plan, q, k_cache, v_cache, out, cu_query_lens, kv_lens,
                                     block_tables, num_blocks, scale, k_scale, v_scale);
-  if (!s.prefill.empty()) {
+  auto run_prefill = [&](cudaStream_t cs) -> ua_status {
     const bool staged = plan->prob.prefill_staged;
     const void* pk = k_cache;
     const void* pv = v_cache;
@@ -517,8 +554,9 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
                            plan->prob.num_kv_heads, cs) != cudaSuccess)
       return UA_ERR_CUDA;
     timing_end(ev, cs);
-  }
-  if (!s.decode.empty()) {
+    return UA_OK;
+  };
+  auto run_decode = [&](cudaStream_t cs) -> ua_status {
     kp.tiles = plan->d_decode;
     kp.num_tiles = static_cast<int32_t>(s.decode.size());
     // split pieces are merged inside the decode launch (last piece per group)
@@ -528,7 +566,30 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     if (ua::launch_decode(kp, plan->prob.head_dim, plan->prob.kv_dtype, cs) != cudaSuccess)
       return UA_ERR_CUDA;
     timing_end(ev, cs);
+    return UA_OK;
+  };
+  if (!s.prefill.empty() && !s.decode.empty()) {
+    if (mp->side == nullptr) {
+      mp->side = side_take(plan->device);
+      if (mp->side == nullptr ||
+          cudaEventCreateWithFlags(&mp->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+          cudaEventCreateWithFlags(&mp->ev_join, cudaEventDisableTiming) != cudaSuccess)
+        return UA_ERR_CUDA;
+    }
+    // fork: the decode half waits for everything queued on the caller's
+    // stream; join: the caller's stream waits for the decode half
+    if (cudaEventRecord(mp->ev_fork, cs) != cudaSuccess ||
+        cudaStreamWaitEvent(mp->side, mp->ev_fork, 0) != cudaSuccess)
+      return UA_ERR_CUDA;
+    const ua_status st_pre = run_prefill(cs);
+    const ua_status st_dec = run_decode(mp->side);
+    if (cudaEventRecord(mp->ev_join, mp->side) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, mp->ev_join, 0) != cudaSuccess)
+      return UA_ERR_CUDA;
+    return st_pre != UA_OK ? st_pre : st_dec;
   }
+  if (!s.prefill.empty()) return run_prefill(cs);
+  if (!s.decode.empty()) return run_decode(cs);
   return UA_OK;
 }
 
