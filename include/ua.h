@@ -41,14 +41,22 @@
  * the "Fused Attention" notes). It replaces the per-program binary search over
  * the query prefix sums that the vLLM kernel performs at run time.
  *
+ * Supported: head_dim 64, 128 (prefill and decode kernels) and 256 (decode
+ * kernel for every sequence); block_size a multiple of 16; any GQA ratio
+ * (the prefill kernel takes ratios dividing 128, other ratios run in the
+ * decode kernel).
+ *
  * Conventions.
  *  - The caller owns every tensor argument; the plan owns its device tile list,
- *    per-plan error word and split workspace (allocated stream-ordered from a
- *    pool the library keeps per device), and frees them in ua_plan_destroy.
+ *    per-plan error word, split workspace and, for an fp8 cache with prefill
+ *    work, a bf16 staging copy of the pages that work reads (all allocated
+ *    stream-ordered from a pool the library keeps per device), and frees them
+ *    in ua_plan_destroy.
  *  - Device pointers must be 16-byte aligned and tensors contiguous.
- *  - All device work is ordered on the stream argument; nothing synchronises
- *    the host except ua_last_device_error, ua_plan_kernel_times and
- *    ua_forward_oneshot.
+ *  - All device work is ordered on the stream argument (a mixed batch's
+ *    decode half runs on a side stream forked from and joined back into it);
+ *    nothing synchronises the host except ua_last_device_error,
+ *    ua_plan_kernel_times and ua_forward_oneshot.
  *  - No entry point calls exit, abort or a device trap. Invalid arguments are
  *    rejected with a negative status before anything is launched.
  */
@@ -130,7 +138,12 @@ typedef struct ua_plan ua_plan;
  * decode tile's key range into min(n, ceil(len/16)) pieces; at most
  * UA_MAX_SPLITS. num_sms <= 0 means 152.
  * decode_rows_max: sequences with q_len * qpk <= this value go to the decode
- * kernel, the others to the prefill kernel; < 0 means the built-in default.
+ * kernel, the others to the prefill kernel (when it takes the problem: head
+ * dim 64 or 128, 128 % qpk == 0, and a bf16 cache with block_size and 128
+ * dividing one another or any fp8 cache); < 0 means the built-in default (32).
+ * The prefill list is in the order the persistent prefill CTAs take it
+ * (grouped by sequence and KV head, the shortest tiles last); the decode list
+ * is longest first.
  */
 ua_status ua_schedule(const int32_t* cu_query_lens_host, const int32_t* kv_lens_host,
                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
@@ -143,8 +156,10 @@ ua_status ua_schedule(const int32_t* cu_query_lens_host, const int32_t* kv_lens_
 
 /*
  * ua_plan_create -- run the scheduler for the current CUDA device and upload
- * the tile lists with one stream-ordered copy; allocates the plan's device
- * memory (tile lists, error word, split workspace).
+ * the tile lists with one stream-ordered copy (from a pinned block the
+ * library recycles, so the host does not wait for earlier work on `stream`);
+ * allocates the plan's device memory (tile lists, error word, split
+ * workspace, fp8 prefill staging) stream-ordered from the library's pool.
  * Arguments as ua_schedule; num_sms is queried from the device.
  * Returns UA_ERR_INVALID_ARG / UA_ERR_UNSUPPORTED for a rejected problem,
  * UA_ERR_CUDA when an allocation or copy fails (nothing is leaked).
