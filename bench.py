@@ -354,6 +354,7 @@ def run_ours(args):
 
     b = tu.to_device(case)
     plan = tu.make_plan(b)
+    plan.set_unified_max(args.unified_max)
     info = plan.info
     out = b.new_out()
     stream = torch.cuda.current_stream()
@@ -455,6 +456,7 @@ def run_ours(args):
             b.kv_lens.copy_(kv_h, non_blocking=True)
             b.block_tables.copy_(bt_h, non_blocking=True)
             with tu.make_plan(b) as p2:
+                p2.set_unified_max(args.unified_max)
                 tu.forward(p2, b, out)
                 out_h.copy_(out, non_blocking=True)
                 torch.cuda.synchronize()
@@ -478,7 +480,8 @@ def run_ours(args):
                    if flush is None else "L2 flushed (256 MB write) between timed steps",
                    "parallelism": "replicas: an independent batch per GPU, no collective",
                    "decode_tiles": info.num_decode_tiles, "prefill_tiles": info.num_prefill_tiles,
-                   "split_tokens": info.split_tokens},
+                   "split_tokens": info.split_tokens,
+                   **({"unified_max": args.unified_max} if args.unified_max is not None else {})},
         "algorithmic": {"bytes_per_step": byts, "flops_per_step": flops},
         "pct_of_peak": (value / world) / (tf_peak if cfg in FLOP_CONFIGS else hbm_peak),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
@@ -690,6 +693,9 @@ def main():
     ap.add_argument("--op", default="attention", choices=["attention", "append"],
                     help="attention: the forward step (default); append: ua_append_kv of the "
                          "step's new K/V")
+    ap.add_argument("--unified-max", type=float, default=None, metavar="PHI",
+                    help="decode rows start from the unified max PHI (scaled-score units) "
+                         "instead of their first maximum (off by default)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

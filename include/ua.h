@@ -270,6 +270,22 @@ ua_status ua_plan_kernel_times(ua_plan* plan, float* ms, int64_t* launches);
  * Both apply to later ua_forward calls on this plan. */
 ua_status ua_plan_set_debug(ua_plan* plan, int32_t flags, int64_t wait_timeout_ns);
 
+/* Unified max for decode work (FlashDecoding++, "Fused Attention" notes:
+ * a preset value stands in for each row's maximum, with a fallback when the
+ * scores leave its range). With enable = 1, every row the decode kernel
+ * processes starts from phi -- in units of the scaled score scale * q.k
+ * (times k_scale for an e4m3 cache), the argument of softmax's exp -- as the
+ * value subtracted before exponentiation, instead of the maximum of its first
+ * keys. Fallback: when the first visible keys' maximum m lies outside
+ * [phi - 64 / log2(e), phi + 8 / log2(e)] (bf16 cache) or
+ * [phi, phi + 8 / log2(e)] (e4m3 cache, whose P operand is f16), or later
+ * keys exceed the reference by more than 8 / log2(e), the row uses its
+ * running maximum, as with enable = 0. The result is the same softmax up to
+ * rounding either way; phi only moves where the rescales happen. Prefill
+ * tiles keep the running maximum. enable = 0 restores the default.
+ * phi must be finite (|phi| <= 1e30); applies to later ua_forward calls. */
+ua_status ua_plan_set_unified_max(ua_plan* plan, int32_t enable, float phi);
+
 /* Synchronises the plan's last stream, reads the device error word
  * (UA_OK, UA_ERR_BOUNDS or UA_ERR_DEVICE_TIMEOUT) into *code and clears it. */
 ua_status ua_last_device_error(ua_plan* plan, int32_t* code);

@@ -34,6 +34,7 @@ EXPORTS = (
     "ua_plan_get_info", "ua_last_device_error", "ua_plan_destroy", "ua_status_string",
     "ua_gather_kv_debug", "ua_plan_set_profiling", "ua_plan_kernel_times",
     "ua_forward_static_scratch", "ua_plan_set_debug", "ua_append_kv",
+    "ua_plan_set_unified_max",
 )
 
 
@@ -90,6 +91,7 @@ _SIGS = {
     "ua_gather_kv_debug": (_I32, [_P, _P, _P, _P, _P, _I64, _P, _P, _I64, _P]),
     "ua_plan_set_profiling": (_I32, [_P, _I32]),
     "ua_plan_set_debug": (_I32, [_P, _I32, _I64]),
+    "ua_plan_set_unified_max": (_I32, [_P, _I32, _F]),
     "ua_forward_static_scratch": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
                                          _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32, _I32, _F,
                                          _F, _I32, _P, _P]),
@@ -245,6 +247,15 @@ def ua_plan_set_debug(plan: int, flags: int, wait_timeout_ns: int = 0):
     _check(lib().ua_plan_set_debug(plan, int(flags), int(wait_timeout_ns)), "ua_plan_set_debug")
 
 
+def ua_plan_set_unified_max(plan: int, phi=None):
+    """Unified max for decode rows (None: off): phi in units of the scaled
+    score; rows whose first maximum lies outside its range fall back to the
+    running maximum."""
+    on = phi is not None
+    _check(lib().ua_plan_set_unified_max(plan, int(on), float(phi) if on else 0.0),
+           "ua_plan_set_unified_max")
+
+
 KERNEL_KINDS = ("prefill", "decode", "combine", "append", "stage")
 
 
@@ -292,6 +303,9 @@ class Plan:
 
     def last_device_error(self) -> int:
         return ua_last_device_error(self.handle)
+
+    def set_unified_max(self, phi=None):
+        ua_plan_set_unified_max(self.handle, phi)
 
     def close(self):
         if self.handle:

@@ -20,7 +20,9 @@
 // keys and head dimensions to lanes so that every 16-byte load is fully
 // coalesced (4 lanes x 16 B of one K row, 8 lanes x 16 B of one V row).
 // Online softmax in base 2 ("Fused Attention" notes, _attn_fwd_inner): running
-// max m, running sum l, rescale factor 2^(m_old - m_new).
+// max m, running sum l, rescale factor 2^(m_old - m_new). Optionally a unified
+// max (FlashDecoding++, "Fused Attention" notes): a preset reference replaces
+// the first step's max, with the running max as the fallback.
 // Four warps per CTA take interleaved 16-key steps of the tile's range and
 // merge their (m, l, O) through shared memory at the end. A split piece
 // leaves its normalised partial and base-2 lse in the workspace; with arrival
@@ -53,6 +55,12 @@ struct DecodeCfg {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+// How far a unified-max reference may sit above a row's first max (log2
+// units): P values down to 2^-64 times the largest are still normal bf16
+// numbers, while f16 P (the e4m3 path) has no range to spare beyond what the
+// running-max path already uses (largest P in [1, 2^8]).
+template <bool FP8>
+constexpr float kUnifiedAbove = FP8 ? 0.0f : 64.0f;
 
 // Key slot (0..15) of a step held as MMA row m of S^T. Chosen so that the
 // PV contraction slots 2t, 2t+1, 2t+8, 2t+9 of lane t are keys 4t..4t+3.
@@ -183,6 +191,7 @@ struct StepMask {
   int pos[2];      // query position of the lane's two rows
   int causal;
   int window;
+  float phi2;      // unified max in log2 units of the scaled score; NaN: off
 };
 
 template <int D, bool FP8>
@@ -237,12 +246,19 @@ __device__ __forceinline__ void compute_step(WarpState<D>& st, StepRegs<D, FP8>&
   // (log2 units 8): P and l use the same stale reference, so the result is
   // exact up to rounding, P stays below 2^8, and the O rescale (a multiply of
   // every accumulator) runs only on the rare steps where some row moved.
+  // With a unified max phi2, a row's first visible step takes phi2 as its
+  // reference when its max lies in [phi2 - kUnifiedAbove, phi2 + 8]; outside
+  // that range (overflow or underflow risk) it falls back to its own max, and
+  // later steps move the reference up as above.
   float p[4], alpha[2];
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
+    const bool first = st.m[j] == -INFINITY;
     const float m_new = fmaxf(st.m[j], mx[j]);
-    const bool grow = (st.m[j] == -INFINITY) || (m_new > st.m[j] + kRescaleThreshold);
-    const float m_use = grow ? m_new : st.m[j];
+    const bool grow = first || (m_new > st.m[j] + kRescaleThreshold);
+    float m_use = grow ? m_new : st.m[j];
+    if (first && mx[j] <= mk.phi2 + kRescaleThreshold && mx[j] >= mk.phi2 - kUnifiedAbove<FP8>)
+      m_use = mk.phi2;
     // Rows with nothing visible yet keep m = -inf; subtract 0 instead so that
     // no -inf - -inf appears.
     const float sub = (m_use == -INFINITY) ? 0.f : m_use;
@@ -409,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
   mk.kv_hi = kv_hi;
   mk.causal = p.causal;
   mk.window = p.window;
+  mk.phi2 = p.unified_max_on ? p.unified_max_log2 : __int_as_float(0x7fc00000);
   {
     const int last = max(nrows - 1, 0);
     const int min_pos = ctx + tile.row0 / p.qpk;

@@ -31,6 +31,28 @@ void key_range(const Problem& p, int32_t ctx, int32_t kv_len, int32_t row0, int3
   *hi = static_cast<int32_t>(h);
 }
 
+// Piece length for decode tiles of (nearly) one key length L: with pieces of
+// about the average slot load, T tiles cut into k pieces each would leave a
+// short last wave (T * k just above a multiple of the CTA slots: e.g. 64
+// tiles of 131072 keys in 8 pieces are 512 CTAs on 456 slots, the last 56
+// holding only 12 % of a tile). Equal pieces run in waves, so the step takes
+// about ceil(T * k / slots) * (L / k + overhead); the k that minimises this
+// (the fewest pieces on a tie) sets the length.
+int64_t wave_fit_chunk(int64_t tiles, int64_t len, int64_t slots) {
+  const int64_t k_max = std::min<int64_t>(UA_MAX_SPLITS, std::max<int64_t>(1, len / kMinSplitTokens));
+  int64_t best_size = len, best_cost = INT64_MAX;
+  for (int64_t k = 1; k <= k_max; ++k) {
+    const int64_t size = round_up(ceil_div(len, k), kKeyStep);
+    const int64_t pieces = ceil_div(len, size);
+    const int64_t cost = ceil_div(tiles * pieces, slots) * (size + kPieceOverheadTokens);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best_size = size;
+    }
+  }
+  return best_size;
+}
+
 }  // namespace
 
 ua_status validate(const Problem& p) {
@@ -119,16 +141,19 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
 
   // 2. Split-KV for decode tiles (FlashDecoding): one chunk length C for the
   // whole batch, so that pieces are equal-sized and load-balance well.
-  int64_t total = 0, longest = 0;
+  int64_t total = 0, longest = 0, shortest = INT64_MAX;
   for (const ua_tile& t : dec) {
     total += t.kv_hi - t.kv_lo;
     longest = std::max<int64_t>(longest, t.kv_hi - t.kv_lo);
+    shortest = std::min<int64_t>(shortest, t.kv_hi - t.kv_lo);
   }
   int64_t chunk = 0;  // 0: do not split
   if (p.num_splits == 0 && !dec.empty() && total > 0) {
-    const int64_t slots = static_cast<int64_t>(num_sms) * kDecodeCtasPerSm;
+    const int64_t slots = static_cast<int64_t>(num_sms) * decode_ctas_per_sm(p.head_dim);
     chunk = round_up(std::max<int64_t>(kMinSplitTokens, ceil_div(total, slots)), kKeyStep);
     chunk = std::max<int64_t>(chunk, round_up(ceil_div(longest, UA_MAX_SPLITS), kKeyStep));
+    if (chunk < longest && shortest * 16 >= longest * 15)
+      chunk = wave_fit_chunk(static_cast<int64_t>(dec.size()), longest, slots);
     if (chunk >= longest) chunk = 0;
   }
   s.split_tokens = static_cast<int32_t>(chunk);

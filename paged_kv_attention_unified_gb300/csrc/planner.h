@@ -63,10 +63,14 @@ struct Schedule {
 // Granularity of key ranges: one decode step reads 16 tokens, so split pieces
 // and decode ranges start on multiples of 16.
 constexpr int kKeyStep = 16;
-// Decode kernel: resident CTAs per SM (three of 64 KB shared memory each),
-// used to size automatic splits: pieces of about the average load of one CTA
-// slot in a single wave, so that long sequences are cut and short ones not.
-constexpr int kDecodeCtasPerSm = 3;
+// Decode kernel: resident CTAs per SM (three of 64 KB shared memory each up
+// to head_dim 128, one at head_dim 256), used to size automatic splits:
+// pieces of about the average load of one CTA slot in a single wave, so that
+// long sequences are cut and short ones not.
+constexpr int decode_ctas_per_sm(int head_dim) { return head_dim > 128 ? 1 : 3; }
+// Cost of one split piece beyond its keys (CTA start, ring fill, merge and
+// store), in key tokens: used when automatic splits are fitted to whole waves.
+constexpr int kPieceOverheadTokens = 128;
 // Smallest automatic split piece, in key tokens.
 constexpr int kMinSplitTokens = 256;
 // Default: sequences with q_len * qpk above this go to the prefill kernel

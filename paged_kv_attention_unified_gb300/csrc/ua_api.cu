@@ -42,6 +42,8 @@ struct ua_plan {
   cudaStream_t last_stream = nullptr;
   int64_t total_q = 0;             // query tokens of the batch (host lengths)
   int32_t debug_flags = 0;         // ua_plan_set_debug
+  bool unified_max_on = false;     // ua_plan_set_unified_max
+  float unified_max = 0.f;
   uint64_t wait_timeout_ns = 2000000000ull;
   // kernel timing (ua_plan_set_profiling)
   struct EventPair {
@@ -254,6 +256,8 @@ ua::KernelParams base_params(const ua_plan* plan, const void* q, const void* k, 
   kp.score_scale_log2 = scale * ua::kLog2e * (fp8 ? k_scale : 1.f);
   kp.v_scale = fp8 ? v_scale : 1.f;
   kp.timeout_ns = plan->wait_timeout_ns;
+  kp.unified_max_on = plan->unified_max_on ? 1 : 0;
+  kp.unified_max_log2 = plan->unified_max * ua::kLog2e;
   return kp;
 }
 
@@ -737,6 +741,14 @@ ua_status ua_plan_set_debug(ua_plan* plan, int32_t flags, int64_t wait_timeout_n
   plan->debug_flags = flags;
   plan->wait_timeout_ns = wait_timeout_ns > 0 ? static_cast<uint64_t>(wait_timeout_ns)
                                               : 2000000000ull;
+  return UA_OK;
+}
+
+ua_status ua_plan_set_unified_max(ua_plan* plan, int32_t enable, float phi) {
+  if (plan == nullptr || (enable != 0 && enable != 1)) return UA_ERR_INVALID_ARG;
+  if (enable && !(std::fabs(phi) <= 1e30f)) return UA_ERR_INVALID_ARG;  // NaN, inf, huge
+  plan->unified_max_on = enable != 0;
+  plan->unified_max = enable ? phi : 0.f;
   return UA_OK;
 }
 

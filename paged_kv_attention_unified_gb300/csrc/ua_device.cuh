@@ -43,6 +43,10 @@ struct KernelParams {
   int32_t* split_counters;
   const ua_combine_group* groups;
   uint64_t timeout_ns;  // bound of every device-side wait
+  // Unified max (FlashDecoding++): when on, the preset reference of every
+  // decode row, in log2 units of the scaled score (phi * log2(e)).
+  int32_t unified_max_on;
+  float unified_max_log2;
 };
 
 struct CombineParams {

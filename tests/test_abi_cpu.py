@@ -90,13 +90,14 @@ def _visible(kv, ql, i, causal, window):
 
 
 def _check_schedule(cu, kv, hq, hkv, causal=1, window=0, num_splits=0, num_sms=152,
-                    decode_rows_max=-1):
-    info, pre, dec, grp = ua.ua_schedule(cu, kv, hq, hkv, 128, 16, 1 + max(kv) // 16 + 1,
+                    decode_rows_max=-1, d=128):
+    info, pre, dec, grp = ua.ua_schedule(cu, kv, hq, hkv, d, 16, 1 + max(kv) // 16 + 1,
                                          causal=causal, window=window, num_splits=num_splits,
                                          num_sms=num_sms, decode_rows_max=decode_rows_max)
     qpk = hq // hkv
-    # the prefill kernel takes bf16 caches with qpk dividing 128 (block size 16 here)
-    prefill_ok = 128 % qpk == 0
+    # the prefill kernel takes bf16 caches with qpk dividing 128 (block size 16
+    # here) at head_dim 64 and 128
+    prefill_ok = 128 % qpk == 0 and d in (64, 128)
     rows_max = (2 ** 63) if not prefill_ok else (32 if decode_rows_max < 0 else decode_rows_max)
     seen = {}
     for kind, tiles, rows_per in (("pre", pre, ua.UA_PREFILL_ROWS), ("dec", dec, 8)):
@@ -266,6 +267,61 @@ def test_prefill_list_ends_with_shortest_tiles(case):
             seen.add(key)
             prev = key
     assert info.num_prefill_ctas == min(152, len(pre))
+
+
+def _piece_lengths(dec):
+    return [t["kv_hi"] - t["kv_lo"] for t in dec]
+
+
+def _waves(n, slots):
+    return -(-n // slots)
+
+
+def test_uniform_decode_splits_fill_whole_waves():
+    """64 (sequence, KV head) tiles of 131072 keys on 152 x 3 CTA slots: the
+    average-load piece (18400 keys) would give 8 pieces per tile, 512 CTAs,
+    whose last 56 hold only the 12 % tails; 7 equal pieces (448 CTAs) run in
+    one wave."""
+    info, _, dec, grp = _check_schedule([0] + list(range(1, 9)), [131072] * 8, 64, 8)
+    assert len(dec) == 448 and _waves(len(dec), 456) == 1
+    lens = _piece_lengths(dec)
+    assert max(lens) - min(lens) <= 16 * 7
+    assert all(g["nsplits"] == 7 for g in grp)
+    # 256 tiles of 8192 keys: the chosen cut beats both the average-load chunk
+    # (2 pieces, 512 CTAs: 2 waves of 4608 keys) and no split (8192 keys)
+    info, _, dec, _ = _check_schedule(list(range(33)), [8192] * 32, 32, 8)
+    lens = _piece_lengths(dec)
+    per_tile = len(dec) // 256
+    assert _waves(len(dec), 456) * (max(lens) + 128) < min(2 * (4608 + 128), 8192 + 128)
+    assert all(g["nsplits"] == per_tile for g in _check_schedule(
+        list(range(33)), [8192] * 32, 32, 8)[3])
+
+
+def test_nonuniform_decode_keeps_the_average_load_chunk():
+    """Lengths that differ by more than 1/16 keep the chunk of about one CTA
+    slot's average load (longest-first order balances the rest)."""
+    import random
+    rng = random.Random(3)
+    kv = [rng.randint(512, 4096) for _ in range(64)]
+    info, _, dec, _ = _check_schedule(list(range(65)), kv, 32, 8)
+    total = 8 * sum(kv)
+    chunk = max(256, -(-total // 456))
+    chunk = -(-chunk // 16) * 16
+    assert info.split_tokens == chunk
+    assert max(_piece_lengths(dec)) == chunk
+
+
+def test_head_dim_256_splits_for_one_cta_per_sm():
+    """At head_dim 256 the decode kernel holds one CTA per SM: uniform pieces
+    are sized for 152 slots (whole waves of 152 CTAs)."""
+    info, _, dec, _ = _check_schedule([0] + list(range(1, 9)), [131072] * 8, 64, 8, d=256)
+    assert len(dec) % 152 == 0 or len(dec) < 152
+
+
+def test_unified_max_rejects_a_null_plan_without_touching_cuda():
+    lib = ua.lib()
+    assert lib.ua_plan_set_unified_max(None, 1, 2.0) == ua.UA_ERR_INVALID_ARG
+    assert lib.ua_plan_set_unified_max(None, 0, 0.0) == ua.UA_ERR_INVALID_ARG
 
 
 def test_append_rejects_a_null_plan_without_touching_cuda():
