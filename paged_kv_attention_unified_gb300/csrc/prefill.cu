@@ -788,7 +788,7 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_
     uint64_t dims[3] = {D, static_cast<uint64_t>(p.num_q_heads), static_cast<uint64_t>(total_q)};
     uint64_t strides[2] = {D * 2, static_cast<uint64_t>(p.num_q_heads) * D * 2};
     uint32_t box[3] = {64, static_cast<uint32_t>(p.qpk), static_cast<uint32_t>(kRows / p.qpk)};
-    cudaError_t e = encode_tiled_map(&mq, 2, 3, q, dims, strides, box, true, false);
+    cudaError_t e = encode_tiled_map(&mq, 2, 3, q, dims, strides, box, true, 128);
     if (e != cudaSuccess) return e;
   }
   // K/V pages: (64 dims, one head, rows_per_box slots, one block) per box.

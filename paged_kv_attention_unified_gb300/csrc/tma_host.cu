@@ -24,7 +24,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 cudaError_t encode_tiled_map(CUtensorMap* map, int elt_bytes, int rank, const void* base,
                              const uint64_t* dims, const uint64_t* strides_bytes,
-                             const uint32_t* box, bool swizzle_128b, bool l2_256b) {
+                             const uint32_t* box, bool swizzle_128b, int l2_promotion) {
   auto encode = encode_fn();
   if (encode == nullptr) return cudaErrorNotSupported;
   cuuint64_t d[5], st[4];
@@ -41,7 +41,9 @@ cudaError_t encode_tiled_map(CUtensorMap* map, int elt_bytes, int rank, const vo
       encode(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, st, b, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE,
              swizzle_128b ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-             l2_256b ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             l2_promotion >= 256   ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+             : l2_promotion >= 128 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                   : CU_TENSOR_MAP_L2_PROMOTION_L2_64B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -56,7 +58,11 @@ cudaError_t encode_kv_page_map(CUtensorMap* map, const void* cache, int elt_byte
   uint64_t strides[3] = {D * e, static_cast<uint64_t>(num_kv_heads) * D * e,
                          static_cast<uint64_t>(block_size) * num_kv_heads * D * e};
   uint32_t box[4] = {static_cast<uint32_t>(box_dims), 1, static_cast<uint32_t>(box_rows), 1};
-  return encode_tiled_map(map, elt_bytes, 4, cache, dims, strides, box, swizzle_128b, true);
+  // L2 fetches no wider than one head's row: the neighbouring head's row
+  // belongs to another CTA, which may read it only after it left L2.
+  const int row_bytes = static_cast<int>(D * e);
+  return encode_tiled_map(map, elt_bytes, 4, cache, dims, strides, box, swizzle_128b,
+                          row_bytes >= 256 ? 256 : (row_bytes >= 128 ? 128 : 64));
 }
 
 }  // namespace ua

@@ -65,14 +65,15 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_
                            int num_kv_heads, cudaStream_t stream);
 
 // Tensor map of a row-major tensor (dims innermost first, strides in bytes of
-// dims 1..rank-1) for bf16 (elt_bytes 2) or byte (elt_bytes 1) elements.
+// dims 1..rank-1) for bf16 (elt_bytes 2) or byte (elt_bytes 1) elements;
+// l2_promotion: L2 fetch width in bytes (64, 128 or 256).
 cudaError_t encode_tiled_map(CUtensorMap* map, int elt_bytes, int rank, const void* base,
                              const uint64_t* dims, const uint64_t* strides_bytes,
-                             const uint32_t* box, bool swizzle_128b, bool l2_256b);
+                             const uint32_t* box, bool swizzle_128b, int l2_promotion);
 
 // Tensor map over a paged cache [num_blocks][block_size][Hkv][head_dim] whose
 // box is (box_dims dims, one head, box_rows slots, one block); an out-of-range
-// block coordinate reads zeros.
+// block coordinate reads zeros. L2 fetches are at most one head row wide.
 cudaError_t encode_kv_page_map(CUtensorMap* map, const void* cache, int elt_bytes, int head_dim,
                                int num_kv_heads, int block_size, int64_t num_blocks,
                                int box_dims, int box_rows, bool swizzle_128b);
