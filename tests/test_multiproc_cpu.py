@@ -87,3 +87,35 @@ def test_reference_arm_nonzero_rank_exits_without_work(monkeypatch, capsys):
 
     assert bench.run_reference(Args()) == 0
     assert capsys.readouterr().out == ""
+
+
+def _reference_line(*extra):
+    import json
+    import subprocess
+    import sys
+    env = dict(os.environ, RANK="0")
+    proc = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                           "--workload", "1", "--steps", "1", "--warmup", "3", *extra],
+                          capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert proc.returncode == 0, proc.stderr[-2000:]
+    lines = [l for l in proc.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, proc.stdout
+    return json.loads(lines[0])
+
+
+@pytest.mark.parametrize("op", ["attention", "append"])
+def test_reference_arm_rank0_prints_one_contract_line(op):
+    """Rank 0 of the reference arm times the oracle on the host (no GPU) and
+    prints the contract line: the same metric keys as the CUDA arm, with
+    cpu_baseline describing the run and a zero-copy e2e."""
+    d = _reference_line("--op", op)
+    assert d["impl"] == "reference"
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "config"):
+        assert k in d, k
+    assert d["value"] > 0 and d["steps"] == 1 and d["warmup"] == 3
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"]
+    assert cb["value"] == d["value"] and cb["unit"] == d["unit"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
