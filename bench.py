@@ -40,6 +40,10 @@ WORKLOAD_NAMES = {
     5: "long decode fp8: 8 seqs, kv 131072, 64/8 heads, d128, fp8 e4m3 KV, bs16",
     6: "dense causal prefill over an fp8 cache: 4 seqs x 4096, 32/32 heads, d128, fp8 e4m3 KV, "
        "bs16, random table (not a benchmark configuration: measures the fp8 prefill path)",
+    7: "uniform decode: 32 seqs, q 1, kv 8192, 32/8 heads, d128, bf16, bs16 (not a benchmark "
+       "configuration: measures split sizing on equal lengths)",
+    8: "pure decode at head_dim 256: 64 seqs, q 1, kv U[512,4096], 32/8 heads, bf16, bs16 "
+       "(not a benchmark configuration: measures the head_dim 256 decode path)",
 }
 FLOP_CONFIGS = (4, 6)   # prefill-bound workloads, reported in TFLOP/s
 
@@ -353,7 +357,7 @@ def run_ours(args):
         cpu = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
 
     b = tu.to_device(case)
-    plan = tu.make_plan(b)
+    plan = tu.make_plan(b, num_splits=args.num_splits)
     plan.set_unified_max(args.unified_max)
     info = plan.info
     out = b.new_out()
@@ -455,7 +459,7 @@ def run_ours(args):
             b.cu_query_lens.copy_(cu_h, non_blocking=True)
             b.kv_lens.copy_(kv_h, non_blocking=True)
             b.block_tables.copy_(bt_h, non_blocking=True)
-            with tu.make_plan(b) as p2:
+            with tu.make_plan(b, num_splits=args.num_splits) as p2:
                 p2.set_unified_max(args.unified_max)
                 tu.forward(p2, b, out)
                 out_h.copy_(out, non_blocking=True)
@@ -481,7 +485,8 @@ def run_ours(args):
                    "parallelism": "replicas: an independent batch per GPU, no collective",
                    "decode_tiles": info.num_decode_tiles, "prefill_tiles": info.num_prefill_tiles,
                    "split_tokens": info.split_tokens,
-                   **({"unified_max": args.unified_max} if args.unified_max is not None else {})},
+                   **({"unified_max": args.unified_max} if args.unified_max is not None else {}),
+                   **({"num_splits": args.num_splits} if args.num_splits else {})},
         "algorithmic": {"bytes_per_step": byts, "flops_per_step": flops},
         "pct_of_peak": (value / world) / (tf_peak if cfg in FLOP_CONFIGS else hbm_peak),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
@@ -693,6 +698,8 @@ def main():
     ap.add_argument("--op", default="attention", choices=["attention", "append"],
                     help="attention: the forward step (default); append: ua_append_kv of the "
                          "step's new K/V")
+    ap.add_argument("--num-splits", type=int, default=0, metavar="N",
+                    help="cut every decode tile into N split pieces (0: automatic sizing)")
     ap.add_argument("--unified-max", type=float, default=None, metavar="PHI",
                     help="decode rows start from the unified max PHI (scaled-score units) "
                          "instead of their first maximum (off by default)")

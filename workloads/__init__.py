@@ -271,6 +271,24 @@ def config6_dense_prefill_fp8(seed: int = 0, poison: bool = False) -> Case:
                      32, 32, 128, 16, kv_dtype=FP8, seed=seed, poison=poison)
 
 
+def config7_uniform_decode(seed: int = 0, poison: bool = False) -> Case:
+    """32 decode sequences of exactly 8192 keys, 32 q / 8 kv heads, d 128,
+    bf16 (not one of the five benchmark configurations: it measures how the
+    automatic split sizing handles a batch of equal lengths)."""
+    return make_case("uniform_decode_b32_kv8192_h32-8_d128_bf16", [1] * 32, [8192] * 32, 32, 8,
+                     128, 16, seed=seed, poison=poison)
+
+
+def config8_pure_decode_d256(seed: int = 0, poison: bool = False) -> Case:
+    """Config 2's batch at head_dim 256: 64 decode sequences, kv_len ~
+    U[512, 4096], 32 q / 8 kv heads, bf16 (not one of the five benchmark
+    configurations: it measures the head_dim 256 decode path)."""
+    gen = torch.Generator().manual_seed(seed)
+    kv = torch.randint(512, 4097, (64,), generator=gen).tolist()
+    return make_case("pure_decode_b64_kv512-4096_h32-8_d256_bf16", [1] * 64, kv, 32, 8, 256, 16,
+                     gen=gen, poison=poison)
+
+
 CONFIGS = {
     1: config1_tiny_mixed,
     2: config2_pure_decode,
@@ -278,6 +296,8 @@ CONFIGS = {
     4: config4_dense_prefill,
     5: config5_long_fp8_decode,
     6: config6_dense_prefill_fp8,
+    7: config7_uniform_decode,
+    8: config8_pure_decode_d256,
 }
 
 
