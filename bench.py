@@ -18,6 +18,7 @@ bounded sample of the same workload, on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -144,7 +145,7 @@ class ClockSampler:
 # CPU oracle timing (baseline; never on the GPU path)
 # ---------------------------------------------------------------------------
 
-def _oracle_worker(cfg, budget_s, seq_limit):
+def _oracle_worker(cfg, budget_s, seq_limit, window=0):
     """Spawned process, one thread: draw the workload, then run the fp64
     oracle sequence by sequence until budget_s of compute has been spent.
     Returns (sequences done, compute seconds)."""
@@ -152,7 +153,7 @@ def _oracle_worker(cfg, budget_s, seq_limit):
         os.environ[v] = "1"
     import oracle
     import workloads as W
-    case = W.CONFIGS[cfg]()
+    case = _with_window(W.CONFIGS[cfg](), window)
     r = case.raw()
     cu = r["cu_query_lens"]
     done, spent = [], 0.0
@@ -195,14 +196,14 @@ def oracle_throughput(cfg, case, budget_s=12.0, seq_limit=1 << 30):
     import multiprocessing as mp
     with concurrent.futures.ProcessPoolExecutor(
             max_workers=1, mp_context=mp.get_context("spawn")) as ex:
-        done, spent = ex.submit(_oracle_worker, cfg, budget_s, seq_limit).result()
+        done, spent = ex.submit(_oracle_worker, cfg, budget_s, seq_limit, case.window).result()
     byts, _ = algorithmic_work(_seq_subcase(case, done))
     sample = (f"{len(done)} of {case.num_seqs} sequences (all heads) of the same workload, "
               f"{spent:.1f} s of single-thread compute")
     return byts / spent / 1e9, 1, sample
 
 
-def _oracle_steps_worker(cfg, steps, step_budget_s):
+def _oracle_steps_worker(cfg, steps, step_budget_s, window=0):
     """Spawned process, one thread: `steps` timed oracle steps, each a run
     over consecutive sequences (cycling) lasting about step_budget_s.
     Returns [(sequence list, seconds)] per step."""
@@ -210,7 +211,7 @@ def _oracle_steps_worker(cfg, steps, step_budget_s):
         os.environ[v] = "1"
     import oracle
     import workloads as W
-    case = W.CONFIGS[cfg]()
+    case = _with_window(W.CONFIGS[cfg](), window)
     r = case.raw()
     cu = r["cu_query_lens"]
     out, s = [], 0
@@ -248,6 +249,11 @@ def _rate(cfg, byts, flops, seconds):
 
 # ---- replicas across ranks (weak scaling: an independent batch per GPU) ----
 
+def _with_window(case, window):
+    """The workload with a left sliding window of `window` keys (0: none)."""
+    return dataclasses.replace(case, window=int(window)) if window else case
+
+
 def rank_case(cfg, rank):
     """This rank's batch: the workload drawn with seed = rank."""
     import workloads as W
@@ -282,14 +288,15 @@ def run_reference(args):
     import concurrent.futures
     import multiprocessing as mp
     cfg = args.workload
-    case = W.CONFIGS[cfg]()
+    case = _with_window(W.CONFIGS[cfg](), getattr(args, "window", 0))
     metric, unit = _metric_for(cfg)
     step_budget = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
     if getattr(args, "op", "attention") == "append":
         return _reference_append(args, case, step_budget)
     with concurrent.futures.ProcessPoolExecutor(
             max_workers=1, mp_context=mp.get_context("spawn")) as ex:
-        res = ex.submit(_oracle_steps_worker, cfg, args.warmup + args.steps, step_budget).result()
+        res = ex.submit(_oracle_steps_worker, cfg, args.warmup + args.steps, step_budget,
+                        case.window).result()
     timed = res[args.warmup:]
     tot_b = tot_f = tot_t = 0.0
     for seqs, secs in timed:
@@ -304,7 +311,8 @@ def run_reference(args):
         "ms_per_step": 1e3 * tot_t / max(1, len(timed)), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
         "data": "synthetic (seeded N(0,1))",
-        "config": {"workload": WORKLOAD_NAMES[cfg], "parallelism": "host, 1 thread"},
+        "config": {"workload": WORKLOAD_NAMES[cfg], "parallelism": "host, 1 thread",
+                   **({"window": case.window} if case.window else {})},
         "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -343,7 +351,7 @@ def run_ours(args):
         dist.init_process_group("nccl")
     B.build()
     cfg = args.workload
-    case = rank_case(cfg, rank)                 # weak scaling: one batch per GPU
+    case = _with_window(rank_case(cfg, rank), args.window)   # weak scaling: one batch per GPU
     byts, flops = algorithmic_work(case)
     metric, unit = _metric_for(cfg)
     hbm_peak, tf_peak, peak_src = _peaks()
@@ -486,7 +494,8 @@ def run_ours(args):
                    "decode_tiles": info.num_decode_tiles, "prefill_tiles": info.num_prefill_tiles,
                    "split_tokens": info.split_tokens,
                    **({"unified_max": args.unified_max} if args.unified_max is not None else {}),
-                   **({"num_splits": args.num_splits} if args.num_splits else {})},
+                   **({"num_splits": args.num_splits} if args.num_splits else {}),
+                   **({"window": args.window} if args.window else {})},
         "algorithmic": {"bytes_per_step": byts, "flops_per_step": flops},
         "pct_of_peak": (value / world) / (tf_peak if cfg in FLOP_CONFIGS else hbm_peak),
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
@@ -698,6 +707,8 @@ def main():
     ap.add_argument("--op", default="attention", choices=["attention", "append"],
                     help="attention: the forward step (default); append: ua_append_kv of the "
                          "step's new K/V")
+    ap.add_argument("--window", type=int, default=0, metavar="W",
+                    help="left sliding window of W keys for the attention step (0: none)")
     ap.add_argument("--num-splits", type=int, default=0, metavar="N",
                     help="cut every decode tile into N split pieces (0: automatic sizing)")
     ap.add_argument("--unified-max", type=float, default=None, metavar="PHI",
