@@ -1,0 +1,74 @@
+"""CPU checks of the benchmark's accounting: the algorithmic bytes and flops
+that every roofline fraction divides by, counted here by brute force over
+(query row, key) pairs, and the oracle baseline path."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+def _brute_work(case):
+    """Visible (query token, key) pairs and the K/V rows any query reads,
+    enumerated one by one from the mask definition."""
+    cu = case.cu_query_lens.tolist()
+    kv = case.kv_lens.tolist()
+    pairs, rows = 0, 0
+    for s in range(case.num_seqs):
+        ql = cu[s + 1] - cu[s]
+        if ql == 0:
+            continue
+        ctx = kv[s] - ql
+        read = set()
+        for i in range(ql):
+            pos = ctx + i
+            for t in range(kv[s]):
+                if case.causal and t > pos:
+                    continue
+                if case.window > 0 and t <= pos - case.window:
+                    continue
+                pairs += 1
+                read.add(t)
+        rows += len(read)
+    return pairs, rows
+
+
+@pytest.mark.parametrize("window,causal", [(0, True), (7, True), (0, False), (40, False)])
+def test_algorithmic_work_matches_brute_force(window, causal):
+    case = W.make_case("acct", [1, 5, 17, 0, 3], [40, 130, 300, 9, 3], 8, 2, 64, 16,
+                       window=window, causal=causal, seed=2)
+    pairs, rows = _brute_work(case)
+    byts, flops = bench.algorithmic_work(case)
+    d, hq, hkv = case.head_dim, case.num_q_heads, case.num_kv_heads
+    tq = int(case.cu_query_lens[-1])
+    pages = sum(-(-k // case.block_size) for q, k in
+                zip((case.cu_query_lens[1:] - case.cu_query_lens[:-1]).tolist(),
+                    case.kv_lens.tolist()) if q > 0)
+    assert flops == 4 * d * hq * pairs
+    assert byts == rows * hkv * d * 2 * 2 + 2 * tq * hq * d * 2 + pages * 4 + \
+        (2 * case.num_seqs + 1) * 4
+
+
+def test_fp8_bytes_count_one_byte_per_element():
+    case = W.make_case("acct8", [1, 2], [100, 37], 16, 2, 128, 16, kv_dtype=W.FP8, seed=3)
+    _, rows = _brute_work(case)
+    byts, _ = bench.algorithmic_work(case)
+    assert byts == rows * 2 * 128 * 1 * 2 + 2 * 3 * 16 * 128 * 2 + (7 + 3) * 4 + 5 * 4
+
+
+def test_window_reduces_the_counted_work():
+    case = W.CONFIGS[1]()
+    full = bench.algorithmic_work(case)
+    win = bench.algorithmic_work(bench._with_window(case, 16))
+    assert win[0] < full[0] and win[1] < full[1]
+    assert bench._with_window(case, 0) is case
+
+
+def test_oracle_baseline_runs_on_the_host():
+    v, cores, sample = bench.oracle_throughput(1, W.CONFIGS[1](), budget_s=0.5)
+    assert v > 0 and cores == 1 and "sequences" in sample
