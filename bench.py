@@ -49,35 +49,46 @@ WORKLOAD_NAMES = {
 FLOP_CONFIGS = (4, 6)   # prefill-bound workloads, reported in TFLOP/s
 
 
-def algorithmic_work(case):
-    """(bytes, flops) one forward must move / compute, counting every visible
-    K/V row once per KV head, Q and the output once, the used page-table
-    entries and the length arrays; flops = 4 * d per (query head, visible key)."""
+def _seq_work(case):
+    """Per sequence: (bytes, flops) of one forward without the length arrays --
+    every visible K/V row once per KV head, Q and the output once, the used
+    page-table entries; flops = 4 * d per (query head, visible key)."""
     cu = case.cu_query_lens.tolist()
     kvl = case.kv_lens.tolist()
     elt = 1 if case.kv_dtype == "fp8_e4m3" else 2
     d, hq, hkv = case.head_dim, case.num_q_heads, case.num_kv_heads
-    kv_rows = 0
-    vis_pairs = 0
-    pages = 0
+    out = []
     for s in range(case.num_seqs):
         ql, kv = cu[s + 1] - cu[s], kvl[s]
         if ql == 0:
+            out.append((0, 0))
             continue
         ctx = kv - ql
         lo = max(0, ctx - case.window + 1) if case.window > 0 else 0
-        kv_rows += kv - lo
-        pages += -(-kv // case.block_size)
+        vis_pairs = 0
         for i in range(ql):
             pos = ctx + i
             hi = pos + 1 if case.causal else kv
             l0 = max(0, pos - case.window + 1) if case.window > 0 else 0
             vis_pairs += hi - l0
-    tq = cu[-1]
-    byts = (kv_rows * hkv * d * elt * 2 + 2 * tq * hq * d * 2 + pages * 4 +
-            (2 * case.num_seqs + 1) * 4)
-    flops = 4 * d * hq * vis_pairs
-    return byts, flops
+        byts = (kv - lo) * hkv * d * elt * 2 + 2 * ql * hq * d * 2 + -(-kv // case.block_size) * 4
+        out.append((byts, 4 * d * hq * vis_pairs))
+    return out
+
+
+def algorithmic_work(case):
+    """(bytes, flops) one forward must move / compute: the per-sequence work
+    of _seq_work plus the two length arrays."""
+    per = _seq_work(case)
+    return (sum(b for b, _ in per) + (2 * case.num_seqs + 1) * 4, sum(f for _, f in per))
+
+
+def units_work(case, units, per=None):
+    """(bytes, flops) of (sequence, KV head) oracle units: each KV head of a
+    sequence carries 1 / Hkv of that sequence's work."""
+    per = per if per is not None else _seq_work(case)
+    h = case.num_kv_heads
+    return (sum(per[s][0] for s, _ in units) / h, sum(per[s][1] for s, _ in units) / h)
 
 
 def _peaks():
@@ -90,15 +101,17 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples during the timed region (read only)."""
+    """nvidia-smi samples (read only) while the block runs; summary() keeps
+    the samples inside the window given by mark_load() / end_load()."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.window = None
 
     def __enter__(self):
         try:
@@ -110,6 +123,13 @@ class ClockSampler:
             self.proc = None
         time.sleep(0.3)
         return self
+
+    def mark_load(self):
+        self.window = [time.time(), None]
+
+    def end_load(self):
+        if self.window:
+            self.window[1] = time.time()
 
     def __exit__(self, *exc):
         self.lines = []
@@ -123,113 +143,75 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        import datetime
+        sm, mx, power, reasons, all_n = [], None, [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for l in getattr(self, "lines", []):
             parts = [p.strip() for p in l.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
+                continue
+            all_n += 1
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            if self.window and ts is not None and not (
+                    self.window[0] - 0.05 <= ts <= (self.window[1] or ts) + 0.05):
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx = float(parts[1])
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+                power.append(float(parts[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
+            for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "samples_total": all_n,
+                "power_w_max": max(power) if power else None,
+                "window_s": (self.window[1] - self.window[0])
+                if self.window and self.window[1] else None}
 
 
 # ---------------------------------------------------------------------------
 # CPU oracle timing (baseline; never on the GPU path)
 # ---------------------------------------------------------------------------
 
-def _oracle_worker(cfg, budget_s, seq_limit, window=0):
-    """Spawned process, one thread: draw the workload, then run the fp64
-    oracle sequence by sequence until budget_s of compute has been spent.
-    Returns (sequences done, compute seconds)."""
-    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[v] = "1"
-    import oracle
-    import workloads as W
-    case = _with_window(W.CONFIGS[cfg](), window)
-    r = case.raw()
-    cu = r["cu_query_lens"]
-    done, spent = [], 0.0
-    for s in range(case.num_seqs):
-        if spent >= budget_s or len(done) >= seq_limit:
-            break
-        t0 = time.perf_counter()
-        oracle.paged_attention(r["q"][cu[s]:cu[s + 1]], r["k_cache"], r["v_cache"],
-                               [0, int(cu[s + 1] - cu[s])], r["kv_lens"][s:s + 1],
-                               r["block_tables"][s:s + 1], case.block_size, case.scale,
-                               kv_dtype=case.kv_dtype, k_scale=case.k_scale,
-                               v_scale=case.v_scale, causal=case.causal, window=case.window)
-        spent += time.perf_counter() - t0
-        done.append(s)
-    return done, spent
+def _oracle_units(case, seed=0):
+    """Every (sequence, KV head) unit of the workload in a seeded random order,
+    so that a time-bounded sample mixes long and short sequences as the
+    workload does."""
+    import random
+    from oracle import pool
+    units = pool.units_of(case.cu_query_lens.tolist(), case.num_kv_heads)
+    random.Random(seed).shuffle(units)
+    return units
 
 
-def _seq_subcase(case, seqs):
-    """A view of `case` restricted to the given sequences (for work counting)."""
-    import torch
-    import workloads as W
-    cu = case.cu_query_lens.tolist()
-    qlens = [cu[s + 1] - cu[s] for s in seqs]
-    new_cu = [0]
-    for q in qlens:
-        new_cu.append(new_cu[-1] + q)
-    return W.Case(name=case.name, q=case.q[:0], k_cache=case.k_cache[:1], v_cache=case.v_cache[:1],
-                  cu_query_lens=torch.tensor(new_cu, dtype=torch.int32),
-                  kv_lens=case.kv_lens[list(seqs)], block_tables=case.block_tables[list(seqs)],
-                  num_q_heads=case.num_q_heads, num_kv_heads=case.num_kv_heads,
-                  head_dim=case.head_dim, block_size=case.block_size, kv_dtype=case.kv_dtype,
-                  scale=case.scale, k_scale=case.k_scale, v_scale=case.v_scale,
-                  causal=case.causal, window=case.window)
-
-
-def oracle_throughput(cfg, case, budget_s=12.0, seq_limit=1 << 30):
-    """Time the oracle (one process, one thread) on whole sequences of the
-    workload for about budget_s; returns (GB/s, cores, sample description)."""
-    import concurrent.futures
-    import multiprocessing as mp
-    with concurrent.futures.ProcessPoolExecutor(
-            max_workers=1, mp_context=mp.get_context("spawn")) as ex:
-        done, spent = ex.submit(_oracle_worker, cfg, budget_s, seq_limit, case.window).result()
-    byts, _ = algorithmic_work(_seq_subcase(case, done))
-    sample = (f"{len(done)} of {case.num_seqs} sequences (all heads) of the same workload, "
-              f"{spent:.1f} s of single-thread compute")
-    return byts / spent / 1e9, 1, sample
-
-
-def _oracle_steps_worker(cfg, steps, step_budget_s, window=0):
-    """Spawned process, one thread: `steps` timed oracle steps, each a run
-    over consecutive sequences (cycling) lasting about step_budget_s.
-    Returns [(sequence list, seconds)] per step."""
-    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        os.environ[v] = "1"
-    import oracle
-    import workloads as W
-    case = _with_window(W.CONFIGS[cfg](), window)
-    r = case.raw()
-    cu = r["cu_query_lens"]
-    out, s = [], 0
-    for _ in range(steps):
-        seqs, spent = [], 0.0
-        while spent < step_budget_s and len(seqs) < case.num_seqs:
-            t0 = time.perf_counter()
-            oracle.paged_attention(r["q"][cu[s]:cu[s + 1]], r["k_cache"], r["v_cache"],
-                                   [0, int(cu[s + 1] - cu[s])], r["kv_lens"][s:s + 1],
-                                   r["block_tables"][s:s + 1], case.block_size, case.scale,
+def oracle_throughput(cfg, case, budget_s=10.0, rounds=1, workers=None):
+    """Time the fp64 oracle on every host core (oracle.pool: one process per
+    core, one thread each) on (sequence, KV head) units of the workload for
+    about budget_s of wall time per round. Returns ([rate per round], cores,
+    sample description, [(bytes, flops, seconds)] per round)."""
+    from oracle import pool
+    per = _seq_work(case)
+    per_round, n = pool.time_units(case.raw(), case.block_size, case.scale, budget_s,
                                    kv_dtype=case.kv_dtype, k_scale=case.k_scale,
                                    v_scale=case.v_scale, causal=case.causal,
-                                   window=case.window)
-            spent += time.perf_counter() - t0
-            seqs.append(s)
-            s = (s + 1) % case.num_seqs
-        out.append((seqs, spent))
-    return out
+                                   window=case.window, workers=workers,
+                                   units=_oracle_units(case), rounds=rounds)
+    rates, raw = [], []
+    for done, wall in per_round:
+        b, f = units_work(case, done, per)
+        rates.append(_rate(cfg, b, f, wall))
+        raw.append((b, f, wall))
+    total_units = case.num_seqs * case.num_kv_heads
+    done0 = per_round[0][0]
+    sample = (f"{len(done0)} (sequence, KV head) units of the same workload "
+              f"({len(set(done0))} distinct of {total_units}, seeded random order) in "
+              f"{per_round[0][1]:.1f} s of wall time on {n} worker processes, one thread each")
+    return rates, n, sample, raw
 
 
 def _metric_for(cfg):
@@ -285,35 +267,32 @@ def run_reference(args):
     if int(os.environ.get("RANK", "0")) != 0:
         return 0
     import workloads as W
-    import concurrent.futures
-    import multiprocessing as mp
     cfg = args.workload
     case = _with_window(W.CONFIGS[cfg](), getattr(args, "window", 0))
     metric, unit = _metric_for(cfg)
-    step_budget = max(0.5, min(3.0, 150.0 / max(1, args.steps + args.warmup)))
+    step_budget = max(0.5, min(2.0, 60.0 / max(1, args.steps + args.warmup)))
     if getattr(args, "op", "attention") == "append":
         return _reference_append(args, case, step_budget)
-    with concurrent.futures.ProcessPoolExecutor(
-            max_workers=1, mp_context=mp.get_context("spawn")) as ex:
-        res = ex.submit(_oracle_steps_worker, cfg, args.warmup + args.steps, step_budget,
-                        case.window).result()
-    timed = res[args.warmup:]
-    tot_b = tot_f = tot_t = 0.0
-    for seqs, secs in timed:
-        b, f = algorithmic_work(_seq_subcase(case, seqs))
-        tot_b, tot_f, tot_t = tot_b + b, tot_f + f, tot_t + secs
+    _, cores, _, raw = oracle_throughput(cfg, case, budget_s=step_budget,
+                                         rounds=args.warmup + args.steps)
+    timed = raw[args.warmup:]
+    tot_b = sum(r[0] for r in timed)
+    tot_f = sum(r[1] for r in timed)
+    tot_t = sum(r[2] for r in timed)
     value = _rate(cfg, tot_b, tot_f, tot_t)
-    sample = (f"each step: consecutive whole sequences (all heads) of the workload for about "
-              f"{step_budget:.1f} s of single-thread fp64 compute")
+    sample = (f"each step: (sequence, KV head) units of the workload in a seeded random order "
+              f"for about {step_budget:.1f} s of wall time on {cores} worker processes "
+              f"(one thread each)")
     line = {
         "impl": "reference", "metric": metric, "value": value, "unit": unit,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / max(1, len(timed)), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (CPU oracle)",
         "data": "synthetic (seeded N(0,1))",
-        "config": {"workload": WORKLOAD_NAMES[cfg], "parallelism": "host, 1 thread",
+        "config": {"workload": WORKLOAD_NAMES[cfg],
+                   "parallelism": f"host, {cores} processes x 1 thread",
                    **({"window": case.window} if case.window else {})},
-        "cpu_baseline": {"value": value, "unit": unit, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -323,46 +302,66 @@ def run_reference(args):
 
 def _traffic_record(kernel: str, cfg: int):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current sources (profiles/traffic.json: {key: {"source_hash", "bytes"}})."""
+    the current sources (profiles/traffic.json: {key: {"source_hash", "bytes"}}).
+    Returns (bytes or None, note, {"current": digest, "record": digest})."""
+    from paged_kv_attention_unified_gb300 import build as B
+    cur = B._digest()
     try:
-        from paged_kv_attention_unified_gb300 import build as B
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(f"{kernel}/workload{cfg}")
-        if rec and rec.get("source_hash") == B._digest():
-            return float(rec["bytes_per_launch"]), rec.get("note")
     except Exception:
-        pass
-    return None, None
+        rec = None
+    digests = {"current": cur, "record": rec.get("source_hash") if rec else None}
+    if rec and rec.get("source_hash") == cur:
+        return float(rec["bytes_per_launch"]), rec.get("note"), digests
+    return None, None, digests
 
 
-def run_ours(args):
+def _timed_steps(n, step, stream, flush):
+    """Device milliseconds of n back-to-back steps: one event pair around all
+    of them, or one per step when the L2 is flushed between steps."""
     import torch
-    import torch.distributed as dist
-    import workloads as W
+    if flush is None:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(n):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1)
+    ms = 0.0
+    for _ in range(n):
+        flush.zero_()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        ms += t0.elapsed_time(t1)
+    return ms
+
+
+def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
+    """One workload through ua_forward: W warm-up steps, a soak of at least
+    soak_s (the same step back to back; gives the sustained rate and the clock
+    record under load), then exactly K timed steps with per-kernel events, the
+    roofline of the dominant kernel, end to end through the C ABI with host
+    buffers, and the oracle on the host cores. Returns the result fields."""
+    import torch
     import paged_kv_attention_unified_gb300 as ua
-    from paged_kv_attention_unified_gb300 import build as B
     from paged_kv_attention_unified_gb300 import torch_utils as tu
 
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl")
-    B.build()
-    cfg = args.workload
     case = _with_window(rank_case(cfg, rank), args.window)   # weak scaling: one batch per GPU
+    per = _seq_work(case)
     byts, flops = algorithmic_work(case)
-    metric, unit = _metric_for(cfg)
     hbm_peak, tf_peak, peak_src = _peaks()
-
-    # CPU baseline first (spawned process, before the timed GPU region).
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, cores, sample = oracle_throughput(cfg, case, budget_s=args.cpu_budget)
-        if cfg in FLOP_CONFIGS:
-            v = v / max(byts, 1) * flops / 1e3  # GB/s -> TFLOP/s on the same sample mix
-        cpu = {"value": v, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
+    if with_cpu:
+        rates, cores, sample, _ = oracle_throughput(cfg, case, budget_s=cpu_budget)
+        cpu = {"value": rates[0], "unit": _metric_for(cfg)[1], "cores": cores, "kind": "oracle",
+               "sample": sample}
 
     b = tu.to_device(case)
     plan = tu.make_plan(b, num_splits=args.num_splits)
@@ -370,44 +369,40 @@ def run_ours(args):
     info = plan.info
     out = b.new_out()
     stream = torch.cuda.current_stream()
-    ua.ua_plan_set_profiling(plan.handle, True)
+    step = lambda: tu.forward(plan, b, out)
+    ua.ua_plan_set_profiling(plan.handle, False)
     for _ in range(args.warmup):
-        tu.forward(plan, b, out)
+        step()
     torch.cuda.synchronize()
-    ua.ua_plan_kernel_times(plan.handle)   # discard warm-up timings
-
-    working_set = byts
     flush = None
-    if working_set < 2 * L2_BYTES:
+    if byts < 2 * L2_BYTES:
         flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        if flush is None:
-            t0 = torch.cuda.Event(enable_timing=True)
-            t1 = torch.cuda.Event(enable_timing=True)
-            t0.record(stream)
-            for _ in range(args.steps):
-                tu.forward(plan, b, out)
-            t1.record(stream)
-            torch.cuda.synchronize()
-            ms = t0.elapsed_time(t1)
-        else:
-            ms = 0.0
-            for _ in range(args.steps):
-                flush.zero_()
-                t0 = torch.cuda.Event(enable_timing=True)
-                t1 = torch.cuda.Event(enable_timing=True)
-                t0.record(stream)
-                tu.forward(plan, b, out)
-                t1.record(stream)
-                torch.cuda.synchronize()
-                ms += t0.elapsed_time(t1)
-    if world > 1:
-        dist.barrier()
+        clk.mark_load()
+        # soak: chunks of about 0.1 s until soak_s has run
+        per_step_ms = max(1e-3, _timed_steps(1, step, stream, flush))
+        chunk = max(1, int(100.0 / per_step_ms))
+        soak_ms, soak_n = 0.0, 0
+        while soak_ms < soak_s * 1e3 or soak_n < args.steps:
+            soak_ms += _timed_steps(chunk, step, stream, flush)
+            soak_n += chunk
+        ua.ua_plan_set_profiling(plan.handle, True)
+        ua.ua_plan_kernel_times(plan.handle)      # synchronises; nothing recorded yet
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ms = _timed_steps(args.steps, step, stream, flush)
+        if world > 1:
+            dist.barrier()
+        clk.end_load()
     ktimes = ua.ua_plan_kernel_times(plan.handle)
+    ua.ua_plan_set_profiling(plan.handle, False)
     ms_max = max_over_ranks(ms, world, device="cuda")
+    soak_max = max_over_ranks(soak_ms / soak_n, world, device="cuda")
     step_s = ms_max / 1e3 / args.steps
     job_bytes = sum_over_ranks(byts, world, device="cuda")
     job_flops = sum_over_ranks(flops, world, device="cuda")
@@ -421,9 +416,10 @@ def run_ours(args):
     _, pre_t, dec_t, _ = ua.ua_schedule(b.cu_host, b.kv_host, b.num_q_heads, b.num_kv_heads,
                                         b.head_dim, b.block_size, int(b.block_tables.shape[1]),
                                         kv_dtype=b.kv_dtype, causal=b.causal, window=b.window,
-                                        num_sms=info.num_sms)
+                                        num_splits=args.num_splits, num_sms=info.num_sms)
     seqs = sorted({t["seq"] for t in (pre_t if kind == "prefill" else dec_t)})
-    k_bytes, k_flops = algorithmic_work(_seq_subcase(case, seqs)) if seqs else (byts, flops)
+    k_bytes = sum(per[s][0] for s in seqs) + (2 * case.num_seqs + 1) * 4
+    k_flops = sum(per[s][1] for s in seqs)
     if kind == "prefill":
         ach = k_flops / avg_s / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
@@ -437,10 +433,17 @@ def run_ours(args):
     roof["kernel"] = kind
     roof["kernel_avg_us"] = avg_s * 1e6
     roof["kernel_share"] = kms / max(1e-9, sum(v[0] for v in ktimes.values()))
-    traffic, note = _traffic_record(kind, cfg)
+    traffic, note, digests = _traffic_record(kind, cfg)
     roof["traffic"] = traffic
     if note:
         roof["traffic_note"] = note
+    else:
+        roof["traffic_digest"] = digests
+    # the whole step against max(bytes / HBM peak, flops / bf16 peak)
+    t_bytes, t_flops = byts / (hbm_peak * 1e9), flops / (tf_peak * 1e12)
+    step_roof = {"bytes_time_us": t_bytes * 1e6, "flops_time_us": t_flops * 1e6,
+                 "bound": "hbm" if t_bytes >= t_flops else "tensor",
+                 "frac": max(t_bytes, t_flops) / (ms_max / 1e3 / args.steps)}
     launches = sum(v[1] for v in ktimes.values())
 
     # end to end through the public API with host buffers, plan included
@@ -451,7 +454,6 @@ def run_ours(args):
         kv_h = case.kv_lens.to(torch.int32).pin_memory()
         bt_h = case.block_tables.to(torch.int32).pin_memory()
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        cu_list, kv_list = case.cu_query_lens.tolist(), case.kv_lens.tolist()
         tiles_b = 32 * (info.num_prefill_tiles + info.num_decode_tiles) + \
             32 * info.num_combine_groups + 16
         h2d = q_h.numel() * 2 + cu_h.numel() * 4 + kv_h.numel() * 4 + bt_h.numel() * 4 + tiles_b
@@ -474,34 +476,84 @@ def run_ours(args):
                 torch.cuda.synchronize()
             if it >= args.warmup:
                 tot += time.perf_counter() - t_0
-        e2e = {"value": _rate(cfg, byts, flops, tot / args.steps), "unit": unit,
+        e2e_s = max_over_ranks(tot / args.steps, world, device="cuda")
+        e2e = {"value": _rate(cfg, job_bytes, job_flops, e2e_s), "unit": _metric_for(cfg)[1],
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "includes": "H2D of q/lengths/page tables, CPU scheduling + tile upload, "
                            "forward, D2H of the output, per step"}
-
     plan.close()
+    del b, out, flush
+    torch.cuda.empty_cache()
+    return {
+        "workload": WORKLOAD_NAMES[cfg], "metric": _metric_for(cfg)[0], "value": value,
+        "unit": _metric_for(cfg)[1], "steps": args.steps, "ms_per_step": ms_max / args.steps,
+        "sustained": {"value": _rate(cfg, job_bytes, job_flops, soak_max / 1e3),
+                      "ms_per_step": soak_max, "steps": soak_n, "seconds": soak_ms / 1e3},
+        "dtype": _dtype_for(case),
+        "l2": ("inputs larger than L2 (%.2f GB > 0.129 GB)" % (byts / 1e9)) if flush is None
+        else "L2 flushed (256 MB write) between timed steps",
+        "tiles": {"decode": info.num_decode_tiles, "prefill": info.num_prefill_tiles,
+                  "split_tokens": info.split_tokens},
+        "algorithmic": {"bytes_per_step": byts, "flops_per_step": flops},
+        "pct_of_peak": (value / world) / (tf_peak if cfg in FLOP_CONFIGS else hbm_peak),
+        "roofline": roof, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(launches), "kernel_ms": {k: v[0] for k, v in ktimes.items()},
+        "clocks": clk.summary(),
+    }
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from paged_kv_attention_unified_gb300 import build as B
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    B.build()
+    cfg = args.workload
+    with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    head = measure_attention(cfg, args, rank, world, with_cpu, args.soak, args.cpu_budget)
+    if args.per_config == "auto":
+        extra = [3, 4, 5] if cfg == 2 and not args.window and not args.num_splits and \
+            args.unified_max is None else []
+    elif args.per_config in ("", "none"):
+        extra = []
+    else:
+        extra = [int(x) for x in args.per_config.split(",") if x]
+    per_config = {}
+    for c in extra:
+        r = measure_attention(c, args, rank, world, with_cpu, args.soak_per_config,
+                              args.cpu_budget_per_config)
+        per_config[str(c)] = r
     if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
         return 0
     line = {
-        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": _dtype_for(case),
-        "data": "synthetic (seeded N(0,1), random page tables)",
-        "config": {"workload": WORKLOAD_NAMES[cfg],
-                   "l2": ("inputs larger than L2 (%.2f GB > 0.129 GB)" % (working_set / 1e9))
-                   if flush is None else "L2 flushed (256 MB write) between timed steps",
+        "metric": head["metric"], "value": head["value"], "unit": head["unit"], "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": head["dtype"], "data": "synthetic (seeded N(0,1), random page tables)",
+        "config": {"workload": head["workload"], "l2": head["l2"],
                    "parallelism": "replicas: an independent batch per GPU, no collective",
-                   "decode_tiles": info.num_decode_tiles, "prefill_tiles": info.num_prefill_tiles,
-                   "split_tokens": info.split_tokens,
+                   "decode_tiles": head["tiles"]["decode"],
+                   "prefill_tiles": head["tiles"]["prefill"],
+                   "split_tokens": head["tiles"]["split_tokens"],
                    **({"unified_max": args.unified_max} if args.unified_max is not None else {}),
                    **({"num_splits": args.num_splits} if args.num_splits else {}),
                    **({"window": args.window} if args.window else {})},
-        "algorithmic": {"bytes_per_step": byts, "flops_per_step": flops},
-        "pct_of_peak": (value / world) / (tf_peak if cfg in FLOP_CONFIGS else hbm_peak),
-        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
-        "kernel_ms": {k: v[0] for k, v in ktimes.items()},
-        "clocks": clk.summary(),
+        "algorithmic": head["algorithmic"], "pct_of_peak": head["pct_of_peak"],
+        "sustained": head["sustained"], "roofline": head["roofline"],
+        "step_roofline": head["step_roofline"], "cpu_baseline": head["cpu_baseline"],
+        "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+        "kernel_ms": head["kernel_ms"], "clocks": head["clocks"],
     }
+    if per_config:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -701,7 +753,18 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOAD_NAMES))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="wall seconds of the oracle on every host core for the headline "
+                         "workload's cpu_baseline")
+    ap.add_argument("--cpu-budget-per-config", type=float, default=4.0)
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of back-to-back steps before the K timed steps (sustained "
+                         "rate and clock record under load)")
+    ap.add_argument("--soak-per-config", type=float, default=0.5)
+    ap.add_argument("--per-config", default="auto",
+                    help="comma-separated workloads measured after the headline one and "
+                         "reported under per_config (auto: 3,4,5 after the default workload 2; "
+                         "none: only the headline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--op", default="attention", choices=["attention", "append"],

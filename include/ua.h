@@ -155,7 +155,13 @@ ua_status ua_schedule(const int32_t* cu_query_lens_host, const int32_t* kv_lens_
                       ua_combine_group* groups, int64_t groups_cap);
 
 /*
- * ua_plan_create -- run the scheduler for the current CUDA device and upload
+ * ua_plan_create -- the CPU work scheduler of the forward. It replaces the
+ * run-time search for each program's sequence over the query prefix sums
+ * (find_seq_idx) and the grid sizing of the host wrapper in
+ * "vllm_triton_unified_attention_notes" (unified_attention section), and
+ * picks the split-KV piece count that run_flash_splitkv_fwd chooses per
+ * launch in "flashatten takeaways EP2 工程" (split-KV launcher section).
+ * Runs the scheduler for the current CUDA device and uploads
  * the tile lists with one stream-ordered copy (from a pinned block the
  * library recycles, so the host does not wait for earlier work on `stream`);
  * allocates the plan's device memory (tile lists, error word, split
@@ -179,7 +185,14 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
                             ua_stream_t stream);
 
 /*
- * ua_forward -- attention for the batch the plan was built for.
+ * ua_forward -- attention for the batch the plan was built for: the boxed
+ * O_{t+1} = softmax(q K^T) V equation of "flashatten takeaways EP2 工程" (kv
+ * cache section) over the paged cache, evaluated tile by tile as
+ * kernel_unified_attention_2d does in "vllm_triton_unified_attention_notes"
+ * (Q tile load, paged K/V load through the block table, causal mask against
+ * the context length, online softmax with running max and sum), with the
+ * online-softmax recurrence of _attn_fwd_inner ("Fused Attention" notes) and
+ * the split-KV log-sum-exp combine (FlashDecoding, same notes).
  * q, k_cache, v_cache, out: device tensors in the layouts above.
  * cu_query_lens, kv_lens, block_tables: device copies. cu_query_lens and
  * kv_lens must hold the values given to the plan; the kernels read them for
@@ -326,11 +339,23 @@ ua_status ua_gather_kv_debug(const ua_plan* plan, const void* k_cache, const voi
  * (one tile per sequence, KV head, block of 8 packed rows and split), and every
  * sequence runs through the split-KV decode kernel and the combine kernel.
  *
+ * Meant for decode-shaped batches (small max_q): the tile grid gives every
+ * sequence ceil(max_q * Hq / Hkv / 8) row blocks, so one long query in the
+ * batch makes every sequence launch that many (mostly empty) decode CTAs;
+ * mixed batches with long prefills belong on ua_forward.
+ *
  * Arguments as ua_forward_oneshot, without host lengths: max_q / max_kv must
  * bound every q_len / kv_len (max_q sizes the tile grid); num_splits 0 picks
  * ceil(max_kv / 1024) pieces (at most UA_MAX_SPLITS, fewer if needed to fit),
- * n > 0 uses exactly n. device_error: optional device int32 that receives the
- * call's error word (UA_OK or UA_ERR_BOUNDS); may be NULL.
+ * n > 0 uses exactly n. scale must be finite; for an e4m3 cache k_scale and
+ * v_scale must be finite and non-zero (else UA_ERR_INVALID_ARG, nothing
+ * launched). device_error: optional device int32 that receives the call's
+ * error word; may be NULL. The word is UA_OK, or UA_ERR_BOUNDS (a page id
+ * outside [0, num_blocks)), UA_ERR_DEVICE_TIMEOUT (a bounded wait of the
+ * decode kernel gave up) or UA_ERR_INVALID_ARG (the device lengths break the
+ * call's bounds: q_len above max_q, kv_len below q_len, or kv_len beyond
+ * max_blocks_per_seq * block_size); the output of the affected rows is then
+ * undefined.
  * Returns UA_ERR_WORKSPACE when the call's scratch (32 B per tile and per
  * group, plus 8 * (head_dim + 1) * 4 B per tile when split) exceeds 16 MiB;
  * nothing is launched then.

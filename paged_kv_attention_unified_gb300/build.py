@@ -41,14 +41,23 @@ def sources():
     return out
 
 
+_SOURCE_SUFFIXES = (".cu", ".cuh", ".cpp", ".h")
+
+
 def _digest(extra=()):
+    """Hash of the library's sources (by file name, not path) and its compile
+    flags with the include paths taken out: the same tree gives the same
+    digest wherever it is checked out (committed ncu traffic records are keyed
+    by it)."""
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)) + sorted(os.listdir(INCLUDE)):
-        base = CSRC if os.path.exists(os.path.join(CSRC, f)) else INCLUDE
-        with open(os.path.join(base, f), "rb") as fh:
-            h.update(f.encode())
+    files = [(f, CSRC) for f in os.listdir(CSRC)] + [(f, INCLUDE) for f in os.listdir(INCLUDE)]
+    for name, base in sorted(files):
+        if not name.endswith(_SOURCE_SUFFIXES):
+            continue
+        with open(os.path.join(base, name), "rb") as fh:
+            h.update(name.encode())
             h.update(fh.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    h.update(" ".join(f for f in NVCC_FLAGS if not f.startswith("-I")).encode())
     for e in extra:
         h.update(str(e).encode())
     return h.hexdigest()

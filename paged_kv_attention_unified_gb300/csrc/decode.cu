@@ -7,18 +7,21 @@
 // merged later by the log-sum-exp combine (FlashDecoding, "Fused Attention"
 // notes; run_flash_splitkv_fwd in "flashatten takeaways EP2 工程").
 //
-// Design for sm_103a. Decode is HBM-bound (about 4-16 flop per cache byte),
-// so the kernel streams K/V pages straight from HBM into registers with
-// 16-byte read-only loads, one step (16 keys) ahead of the math, and keeps
-// the math on the tensor pipe with m16n8k16 MMAs in a transposed orientation:
+// Design for sm_103a. Decode is HBM-bound (about 4-16 flop per cache byte).
+// Each warp owns a ring of shared-memory stages; one lane issues, per 16-key
+// step, one TMA box of K and one of V (the 16 slots of one KV head in one
+// page) a few steps ahead of the math, and the warp reads the landed page
+// into registers and keeps the math on the tensor pipe with m16n8k16 MMAs in
+// a transposed orientation:
 //   S^T[key, row]  = K[key, :] . Q[row, :]      (M = 16 keys, N = 8 rows)
 //   O^T[d, row]   += V^T[d, key] . P^T[key, row] (M = 16 dims, N = 8 rows)
 // Keys on M and the GQA rows on N waste no MMA rows when 8 query heads share
 // a KV head. The score fragment becomes the PV operand with one movmatrix
 // transpose per 8x8 block. Because the contraction index of both products
 // and the M index of the second may be permuted freely, the kernel assigns
-// keys and head dimensions to lanes so that every 16-byte load is fully
-// coalesced (4 lanes x 16 B of one K row, 8 lanes x 16 B of one V row).
+// keys and head dimensions to lanes so that the shared-memory fragment reads
+// take the minimum number of wavefronts (4 lanes x 16 B of one K row, 8 lanes
+// x 16 B of one V row, with the 128-byte swizzle of the staged page).
 // Online softmax in base 2 ("Fused Attention" notes, _attn_fwd_inner): running
 // max m, running sum l, rescale factor 2^(m_old - m_new). Optionally a unified
 // max (FlashDecoding++, "Fused Attention" notes): a preset reference replaces

@@ -15,6 +15,7 @@
 // are then run by the same decode and combine kernels as ua_forward.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "ua_kernels.h"
@@ -73,10 +74,15 @@ cudaError_t scratch_on_device(int dev, unsigned char** out) {
 // s see keys up to ctx + last token (causal) and above the window; the range,
 // starting on a multiple of 16, is cut into `splits` equal pieces of a
 // multiple of 16 keys. Rows or pieces that do not exist become empty tiles.
+// The grid covers max_q tokens per sequence; one thread per sequence records
+// UA_ERR_INVALID_ARG in the error word when the device lengths break the
+// call's bounds (more packed rows than the grid holds, kv_len < q_len, or a
+// kv_len past the page table), since those rows would otherwise be left
+// unwritten or silently masked.
 __global__ void build_tiles_kernel(const int32_t* cu_query_lens, const int32_t* kv_lens,
                                    int num_seqs, int num_kv_heads, int qpk, int row_tiles,
-                                   int splits, int causal, int window, ua_tile* tiles,
-                                   ua_combine_group* groups) {
+                                   int splits, int causal, int window, int64_t max_keys,
+                                   ua_tile* tiles, ua_combine_group* groups, int32_t* err) {
   const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t total = static_cast<int64_t>(num_seqs) * num_kv_heads * row_tiles * splits;
   if (n >= total) return;
@@ -89,6 +95,11 @@ __global__ void build_tiles_kernel(const int32_t* cu_query_lens, const int32_t* 
   const int kv = kv_lens[s];
   const int rows = qlen * qpk;
   const int row0 = rt * UA_DECODE_ROWS;
+  if (g == 0 && rt == 0 && j == 0 &&
+      (qlen < 0 || kv < qlen || static_cast<int64_t>(qlen) * qpk >
+                                    static_cast<int64_t>(row_tiles) * UA_DECODE_ROWS ||
+       kv > max_keys))
+    record_error(err, UA_ERR_INVALID_ARG);
   const int nrows = max(0, min(UA_DECODE_ROWS, rows - row0));
   int lo = 0, hi = 0;
   if (nrows > 0) {
@@ -155,6 +166,10 @@ extern "C" ua_status ua_forward_static_scratch(
   auto misaligned = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; };
   if (misaligned(q) || misaligned(k_cache) || misaligned(v_cache) || misaligned(out))
     return UA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return UA_ERR_INVALID_ARG;
+  if (kv_dtype == UA_KV_FP8_E4M3 && (!std::isfinite(k_scale) || !std::isfinite(v_scale) ||
+                                     k_scale == 0.f || v_scale == 0.f))
+    return UA_ERR_INVALID_ARG;
 
   const int qpk = num_q_heads / num_kv_heads;
   const int64_t row_tiles = (static_cast<int64_t>(max_q) * qpk + UA_DECODE_ROWS - 1) / UA_DECODE_ROWS;
@@ -188,7 +203,8 @@ extern "C" ua_status ua_forward_static_scratch(
   const int threads = 256;
   build_tiles_kernel<<<static_cast<unsigned>((tiles + threads - 1) / threads), threads, 0, cs>>>(
       cu_query_lens, kv_lens, num_seqs, num_kv_heads, qpk, static_cast<int>(row_tiles), splits,
-      causal, window, d_tiles, d_groups);
+      causal, window, static_cast<int64_t>(max_blocks_per_seq) * block_size, d_tiles, d_groups,
+      d_err);
   if (cudaGetLastError() != cudaSuccess) return UA_ERR_CUDA;
 
   KernelParams kp{};

@@ -20,13 +20,15 @@ def oracle_full(case):
     return out
 
 
-def oracle_rows(case, rows):
+def oracle_full_parallel(case):
+    """The whole-batch oracle output, computed (sequence, KV head) unit by unit
+    on every host core (oracle.pool): for the full-size workloads."""
+    from oracle import pool
     r = case.raw()
-    out, _ = oracle.paged_attention_rows(r["q"], r["k_cache"], r["v_cache"], r["cu_query_lens"],
-                                         r["kv_lens"], r["block_tables"], case.block_size,
-                                         case.scale, rows, kv_dtype=case.kv_dtype,
-                                         k_scale=case.k_scale, v_scale=case.v_scale,
-                                         causal=case.causal, window=case.window)
+    out, _ = pool.paged_attention_parallel(r, case.block_size, case.scale,
+                                           kv_dtype=case.kv_dtype, k_scale=case.k_scale,
+                                           v_scale=case.v_scale, causal=case.causal,
+                                           window=case.window)
     return out
 
 
@@ -34,29 +36,22 @@ def as_f64(t: torch.Tensor) -> np.ndarray:
     return t.to(torch.float64).cpu().numpy()
 
 
-def assert_close(got: np.ndarray, exp: np.ndarray, kv_dtype: str, what: str = ""):
+# (what, elements compared, max-abs, mean-abs) of every comparison flagged
+# for the report; tests/conftest.py prints them at the end of the run.
+PARITY_REPORT = []
+
+
+def assert_close(got: np.ndarray, exp: np.ndarray, kv_dtype: str, what: str = "",
+                 report: bool = False):
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert got.shape == exp.shape, f"{what}: shape {got.shape} vs {exp.shape}"
     err = np.abs(got - exp)
     mx, mean = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
+    if report:
+        PARITY_REPORT.append((what, int(err.size), mx, mean))
     if kv_dtype == W.FP8:
         assert mx <= FP8_MAX_ABS, f"{what}: max-abs {mx:.3e} > {FP8_MAX_ABS}"
     else:
         assert mx <= BF16_MAX_ABS, f"{what}: max-abs {mx:.3e} > {BF16_MAX_ABS}"
         assert mean <= BF16_MEAN_ABS, f"{what}: mean-abs {mean:.3e} > {BF16_MEAN_ABS}"
     return mx, mean
-
-
-def sample_rows(case, n, seed=0):
-    """n (token, head) rows spread over every sequence, including first and last tokens."""
-    rng = np.random.default_rng(seed)
-    cu = case.cu_query_lens.tolist()
-    rows = []
-    B = case.num_seqs
-    for k in range(n):
-        s = k % B if k < 2 * B else int(rng.integers(B))
-        ql = cu[s + 1] - cu[s]
-        if ql == 0:
-            continue
-        i = [0, ql - 1][k % 2] if k < 2 * B else int(rng.integers(ql))
-        rows.append((cu[s] + i, int(rng.integers(case.num_q_heads))))
-    return rows

@@ -69,6 +69,23 @@ def test_window_reduces_the_counted_work():
     assert bench._with_window(case, 0) is case
 
 
-def test_oracle_baseline_runs_on_the_host():
-    v, cores, sample = bench.oracle_throughput(1, W.CONFIGS[1](), budget_s=0.5)
-    assert v > 0 and cores == 1 and "sequences" in sample
+def test_oracle_baseline_runs_on_every_host_core():
+    rates, cores, sample, raw = bench.oracle_throughput(1, W.CONFIGS[1](), budget_s=0.5,
+                                                        rounds=2)
+    assert len(rates) == 2 and all(v > 0 for v in rates)
+    assert cores == len(os.sched_getaffinity(0)) and "units" in sample
+    assert all(b > 0 and f > 0 and t > 0 for b, f, t in raw)
+
+
+@pytest.mark.parametrize("window", [0, 40])
+def test_unit_work_adds_up_to_the_whole_forward(window):
+    """The oracle baseline credits each (sequence, KV head) unit with 1/Hkv of
+    its sequence's work: over all units that is the whole forward minus the
+    length arrays."""
+    case = bench._with_window(W.make_case("units", [1, 30, 4], [700, 30, 90], 16, 4, 64, 16,
+                                          seed=4), window)
+    from oracle import pool
+    units = pool.units_of(case.cu_query_lens.tolist(), 4)
+    b, f = bench.units_work(case, units)
+    tb, tf = bench.algorithmic_work(case)
+    assert b == tb - (2 * 3 + 1) * 4 and f == tf

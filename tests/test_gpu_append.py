@@ -9,7 +9,7 @@ import paged_kv_attention_unified_gb300 as ua
 from paged_kv_attention_unified_gb300 import torch_utils as tu
 import workloads as W
 
-from _helpers import as_f64, assert_close, oracle_full, sample_rows, oracle_rows
+from _helpers import as_f64, assert_close, oracle_full
 
 pytestmark = pytest.mark.gpu
 

@@ -392,3 +392,28 @@ def test_mutation_combine_weight_is_caught(monkeypatch):
     assert np.max(np.abs(wrong_out - o_ref)) > 1e-6
     o, _ = oracle.combine_partials(outs, lses)
     assert np.max(np.abs(o - o_ref)) <= 1e-12
+
+
+def test_pooled_oracle_equals_the_whole_batch_oracle():
+    """oracle.pool cuts a batch into (sequence, KV head) units run in spawned
+    processes; the assembled result is the whole-batch definition (GQA groups,
+    windows, non-causal masks and fp8 scales included)."""
+    from oracle import pool
+    cases = [W.config1_tiny_mixed(),
+             W.random_small_case(3, kv_dtype=W.FP8, num_q_heads=16, num_kv_heads=4, window=50),
+             W.random_small_case(7, causal=False, num_q_heads=6, num_kv_heads=2)]
+    for case in cases:
+        r = case.raw()
+        kw = dict(kv_dtype=case.kv_dtype, k_scale=case.k_scale, v_scale=case.v_scale,
+                  causal=case.causal, window=case.window)
+        a, la = oracle.paged_attention(r["q"], r["k_cache"], r["v_cache"], r["cu_query_lens"],
+                                       r["kv_lens"], r["block_tables"], case.block_size,
+                                       case.scale, **kw)
+        b, lb = pool.paged_attention_parallel(r, case.block_size, case.scale, workers=3, **kw)
+        np.testing.assert_allclose(b, a, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lb, la, rtol=0, atol=1e-12)
+    per_round, n = pool.time_units(cases[0].raw(), 16, 0.125, 0.2, workers=2, rounds=2)
+    assert n == 2 and len(per_round) == 2
+    for done, wall in per_round:
+        assert wall > 0 and len(done) >= 1
+        assert set(done) <= set(pool.units_of(cases[0].cu_query_lens.numpy(), 4))
