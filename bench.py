@@ -366,6 +366,8 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
     b = tu.to_device(case)
     plan = tu.make_plan(b, num_splits=args.num_splits)
     plan.set_unified_max(args.unified_max)
+    if args.prefill_ctas:
+        ua.ua_plan_set_prefill_ctas(plan.handle, args.prefill_ctas)
     info = plan.info
     out = b.new_out()
     stream = torch.cuda.current_stream()
@@ -408,42 +410,57 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
     job_flops = sum_over_ranks(flops, world, device="cuda")
     value = _rate(cfg, job_bytes, job_flops, step_s)
 
-    # dominant kernel and its roofline, credited with the work of the sequences
-    # the scheduler gave it (host-only schedule of the same batch)
-    kind = max(("prefill", "decode"), key=lambda k: ktimes[k][0])
-    kms, kn = ktimes[kind]
-    avg_s = kms / 1e3 / max(kn, 1)
-    _, pre_t, dec_t, _ = ua.ua_schedule(b.cu_host, b.kv_host, b.num_q_heads, b.num_kv_heads,
-                                        b.head_dim, b.block_size, int(b.block_tables.shape[1]),
-                                        kv_dtype=b.kv_dtype, causal=b.causal, window=b.window,
-                                        num_splits=args.num_splits, num_sms=info.num_sms)
-    seqs = sorted({t["seq"] for t in (pre_t if kind == "prefill" else dec_t)})
-    k_bytes = sum(per[s][0] for s in seqs) + (2 * case.num_seqs + 1) * 4
-    k_flops = sum(per[s][1] for s in seqs)
-    if kind == "prefill":
-        ach = k_flops / avg_s / 1e12
-        roof = {"bound": "tensor", "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
-                "frac": ach / tf_peak, "work_per_launch": k_flops}
-    else:
-        ach = k_bytes / avg_s / 1e9
-        roof = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                "frac": ach / hbm_peak, "work_per_launch": k_bytes}
-    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" \
-        else "fallback"
-    roof["kernel"] = kind
-    roof["kernel_avg_us"] = avg_s * 1e6
-    roof["kernel_share"] = kms / max(1e-9, sum(v[0] for v in ktimes.values()))
-    traffic, note, digests = _traffic_record(kind, cfg)
-    roof["traffic"] = traffic
-    if note:
-        roof["traffic_note"] = note
-    else:
-        roof["traffic_digest"] = digests
     # the whole step against max(bytes / HBM peak, flops / bf16 peak)
     t_bytes, t_flops = byts / (hbm_peak * 1e9), flops / (tf_peak * 1e12)
     step_roof = {"bytes_time_us": t_bytes * 1e6, "flops_time_us": t_flops * 1e6,
                  "bound": "hbm" if t_bytes >= t_flops else "tensor",
                  "frac": max(t_bytes, t_flops) / (ms_max / 1e3 / args.steps)}
+    # each kernel's roofline, credited with the work of the sequences the
+    # scheduler gave it (host-only schedule of the same batch)
+    _, pre_t, dec_t, _ = ua.ua_schedule(b.cu_host, b.kv_host, b.num_q_heads, b.num_kv_heads,
+                                        b.head_dim, b.block_size, int(b.block_tables.shape[1]),
+                                        kv_dtype=b.kv_dtype, causal=b.causal, window=b.window,
+                                        num_splits=args.num_splits, num_sms=info.num_sms)
+    mixed = bool(pre_t) and bool(dec_t)
+    rooflines = {}
+    for kind, tiles in (("prefill", pre_t), ("decode", dec_t)):
+        kms, kn = ktimes[kind]
+        if not tiles or kn == 0:
+            continue
+        avg_s = kms / 1e3 / kn
+        seqs = sorted({t["seq"] for t in tiles})
+        k_bytes = sum(per[s][0] for s in seqs) + (2 * case.num_seqs + 1) * 4
+        k_flops = sum(per[s][1] for s in seqs)
+        if kind == "prefill":
+            ach = k_flops / avg_s / 1e12
+            r = {"bound": "tensor", "achieved": ach, "peak": tf_peak, "unit": "TFLOP/s",
+                 "frac": ach / tf_peak, "work_per_launch": k_flops}
+        else:
+            ach = k_bytes / avg_s / 1e9
+            r = {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                 "frac": ach / hbm_peak, "work_per_launch": k_bytes}
+        r["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" \
+            if peak_src == "measured" else "fallback"
+        r["kernel"] = kind
+        r["kernel_avg_us"] = avg_s * 1e6
+        r["kernel_share"] = kms / max(1e-9, sum(v[0] for v in ktimes.values()))
+        r["timing"] = ("device global-timer span, first CTA start to last CTA end (the two "
+                       "kernels of a mixed step overlap)") if mixed else \
+            "CUDA events on the launching stream"
+        traffic, note, digests = _traffic_record(kind, cfg)
+        r["traffic"] = traffic
+        if note:
+            r["traffic_note"] = note
+        else:
+            r["traffic_digest"] = digests
+        rooflines[kind] = r
+    # the dominant kernel: the one whose bound is the step's (a mixed step
+    # runs both kernels at once), else the only one
+    want = "decode" if step_roof["bound"] == "hbm" else "prefill"
+    kind = want if want in rooflines else next(iter(rooflines))
+    roof = dict(rooflines[kind])
+    if len(rooflines) > 1:
+        roof["other_kernels"] = {k: v for k, v in rooflines.items() if k != kind}
     launches = sum(v[1] for v in ktimes.values())
 
     # end to end through the public API with host buffers, plan included
@@ -471,6 +488,8 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
             b.block_tables.copy_(bt_h, non_blocking=True)
             with tu.make_plan(b, num_splits=args.num_splits) as p2:
                 p2.set_unified_max(args.unified_max)
+                if args.prefill_ctas:
+                    ua.ua_plan_set_prefill_ctas(p2.handle, args.prefill_ctas)
                 tu.forward(p2, b, out)
                 out_h.copy_(out, non_blocking=True)
                 torch.cuda.synchronize()
@@ -482,6 +501,8 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
                "includes": "H2D of q/lengths/page tables, CPU scheduling + tile upload, "
                            "forward, D2H of the output, per step"}
     plan.close()
+    l2_note = ("inputs larger than L2 (%.2f GB > 0.129 GB)" % (byts / 1e9)) if flush is None \
+        else "L2 flushed (256 MB write) between timed steps"
     del b, out, flush
     torch.cuda.empty_cache()
     return {
@@ -490,10 +511,10 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
         "sustained": {"value": _rate(cfg, job_bytes, job_flops, soak_max / 1e3),
                       "ms_per_step": soak_max, "steps": soak_n, "seconds": soak_ms / 1e3},
         "dtype": _dtype_for(case),
-        "l2": ("inputs larger than L2 (%.2f GB > 0.129 GB)" % (byts / 1e9)) if flush is None
-        else "L2 flushed (256 MB write) between timed steps",
+        "l2": l2_note,
         "tiles": {"decode": info.num_decode_tiles, "prefill": info.num_prefill_tiles,
-                  "split_tokens": info.split_tokens},
+                  "split_tokens": info.split_tokens,
+                  "prefill_ctas": args.prefill_ctas or info.num_prefill_ctas},
         "algorithmic": {"bytes_per_step": byts, "flops_per_step": flops},
         "pct_of_peak": (value / world) / (tf_peak if cfg in FLOP_CONFIGS else hbm_peak),
         "roofline": roof, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
@@ -519,7 +540,7 @@ def run_ours(args):
     head = measure_attention(cfg, args, rank, world, with_cpu, args.soak, args.cpu_budget)
     if args.per_config == "auto":
         extra = [3, 4, 5] if cfg == 2 and not args.window and not args.num_splits and \
-            args.unified_max is None else []
+            args.unified_max is None and not args.prefill_ctas else []
     elif args.per_config in ("", "none"):
         extra = []
     else:
@@ -543,6 +564,7 @@ def run_ours(args):
                    "decode_tiles": head["tiles"]["decode"],
                    "prefill_tiles": head["tiles"]["prefill"],
                    "split_tokens": head["tiles"]["split_tokens"],
+                   "prefill_ctas": head["tiles"]["prefill_ctas"],
                    **({"unified_max": args.unified_max} if args.unified_max is not None else {}),
                    **({"num_splits": args.num_splits} if args.num_splits else {}),
                    **({"window": args.window} if args.window else {})},
@@ -774,6 +796,8 @@ def main():
                     help="left sliding window of W keys for the attention step (0: none)")
     ap.add_argument("--num-splits", type=int, default=0, metavar="N",
                     help="cut every decode tile into N split pieces (0: automatic sizing)")
+    ap.add_argument("--prefill-ctas", type=int, default=0, metavar="P",
+                    help="persistent prefill CTAs of a mixed step (0: the scheduler's choice)")
     ap.add_argument("--unified-max", type=float, default=None, metavar="PHI",
                     help="decode rows start from the unified max PHI (scaled-score units) "
                          "instead of their first maximum (off by default)")

@@ -121,8 +121,11 @@ typedef struct {
   int64_t workspace_bytes;     /* bytes of split workspace the plan owns */
   int32_t split_tokens;        /* key tokens per split piece (0: no splits) */
   int32_t num_sms;             /* SM count the schedule was sized for */
-  int32_t num_prefill_ctas;    /* CTAs of the persistent prefill launch: min(num_sms, prefill
-                                  tiles); they take the prefill tiles in list order */
+  int32_t num_prefill_ctas;    /* CTAs of the persistent prefill launch, one per SM; they take
+                                  the prefill tiles in list order. min(num_sms, prefill tiles)
+                                  without decode tiles; with decode tiles too, the count that
+                                  balances the two kernels (the decode kernel takes the other
+                                  SMs while the prefill runs) */
   int32_t reserved;            /* zero */
 } ua_plan_info;
 
@@ -206,9 +209,11 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
  * Launches the prefill kernel (after the staging kernel for an fp8 cache)
  * and the decode kernel (which merges split pieces itself) in the order of
  * `stream`: when the batch has both, the decode kernel runs on a side stream
- * of the library's pool that starts after everything queued on `stream` and
- * that `stream` waits for, so that the two kernels share the GPU; work queued
- * on `stream` afterwards sees the whole result. Not thread-safe per plan:
+ * of the library's pool that starts once every prefill CTA has begun (so
+ * after everything queued on `stream` before the call) and that `stream`
+ * waits for: the prefill CTAs hold num_prefill_ctas SMs and the decode CTAs
+ * stream the cache on the others, then on the prefill SMs as they free up.
+ * Work queued on `stream` afterwards sees the whole result. Not thread-safe per plan:
  * calls that share a plan must be ordered (they share its split workspace).
  */
 ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
@@ -266,11 +271,15 @@ ua_status ua_plan_get_info(const ua_plan* plan, ua_plan_info* info);
 
 /* Kernel timing for measurement tools. While enabled, ua_forward and
  * ua_append_kv record a CUDA event pair on their stream around each kernel
- * launch (a few microseconds per launch); ua_plan_kernel_times synchronises,
- * sums the elapsed milliseconds and launch counts per kernel kind since the
- * last read -- index 0 prefill, 1 decode, 2 combine, 3 append, 4 fp8
- * prefill staging -- into ms[0..UA_KERNEL_KINDS-1] /
- * launches[0..UA_KERNEL_KINDS-1], and clears them. */
+ * launch (a few microseconds per launch). The exception is a batch with both
+ * prefill and decode tiles, whose two kernels overlap: there each of the two
+ * records its own span instead (first CTA start to last CTA end, device
+ * global timer), so that no event sits between the launches.
+ * ua_plan_kernel_times synchronises, sums the elapsed milliseconds and launch
+ * counts per kernel kind since the last read -- index 0 prefill, 1 decode,
+ * 2 combine, 3 append, 4 fp8 prefill staging -- into ms[0..UA_KERNEL_KINDS-1]
+ * / launches[0..UA_KERNEL_KINDS-1], and clears them. Up to 1024 self-timed
+ * launches are kept between reads; later ones are not counted. */
 #define UA_KERNEL_KINDS 5
 ua_status ua_plan_set_profiling(ua_plan* plan, int32_t enable);
 ua_status ua_plan_kernel_times(ua_plan* plan, float* ms, int64_t* launches);
@@ -298,6 +307,12 @@ ua_status ua_plan_set_debug(ua_plan* plan, int32_t flags, int64_t wait_timeout_n
  * tiles keep the running maximum. enable = 0 restores the default.
  * phi must be finite (|phi| <= 1e30); applies to later ua_forward calls. */
 ua_status ua_plan_set_unified_max(ua_plan* plan, int32_t enable, float phi);
+
+/* Tuning aid: run the prefill kernel of later ua_forward calls on this plan
+ * with num_ctas persistent CTAs (capped at the SM count and the prefill tile
+ * count) instead of the scheduler's num_prefill_ctas; 0 restores it. Results
+ * do not depend on it. */
+ua_status ua_plan_set_prefill_ctas(ua_plan* plan, int32_t num_ctas);
 
 /* Synchronises the plan's last stream, reads the device error word
  * (UA_OK, UA_ERR_BOUNDS or UA_ERR_DEVICE_TIMEOUT) into *code and clears it. */

@@ -34,7 +34,7 @@ EXPORTS = (
     "ua_plan_get_info", "ua_last_device_error", "ua_plan_destroy", "ua_status_string",
     "ua_gather_kv_debug", "ua_plan_set_profiling", "ua_plan_kernel_times",
     "ua_forward_static_scratch", "ua_plan_set_debug", "ua_append_kv",
-    "ua_plan_set_unified_max",
+    "ua_plan_set_unified_max", "ua_plan_set_prefill_ctas",
 )
 
 
@@ -92,6 +92,7 @@ _SIGS = {
     "ua_plan_set_profiling": (_I32, [_P, _I32]),
     "ua_plan_set_debug": (_I32, [_P, _I32, _I64]),
     "ua_plan_set_unified_max": (_I32, [_P, _I32, _F]),
+    "ua_plan_set_prefill_ctas": (_I32, [_P, _I32]),
     "ua_forward_static_scratch": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
                                          _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32, _I32, _F,
                                          _F, _I32, _P, _P]),
@@ -245,6 +246,11 @@ def ua_plan_set_profiling(plan: int, enable: bool):
 def ua_plan_set_debug(plan: int, flags: int, wait_timeout_ns: int = 0):
     """Test aid: flags bit 0 idles the prefill producer (bounded waits run out)."""
     _check(lib().ua_plan_set_debug(plan, int(flags), int(wait_timeout_ns)), "ua_plan_set_debug")
+
+
+def ua_plan_set_prefill_ctas(plan: int, num_ctas: int = 0):
+    """Prefill CTAs of later forwards on this plan (0: the scheduler's count)."""
+    _check(lib().ua_plan_set_prefill_ctas(plan, int(num_ctas)), "ua_plan_set_prefill_ctas")
 
 
 def ua_plan_set_unified_max(plan: int, phi=None):

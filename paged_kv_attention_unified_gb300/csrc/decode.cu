@@ -343,6 +343,10 @@ __global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
   const ua_tile tile = p.tiles[blockIdx.x];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
+  if (threadIdx.x == 0 && p.span_start != nullptr) atomicMin(p.span_start, sm100::globaltimer_ns());
+  auto stamp_end = [&]() {
+    if (threadIdx.x == 0 && p.span_end != nullptr) atomicMax(p.span_end, sm100::globaltimer_ns());
+  };
   if (threadIdx.x == 0) {
     *never = 0;
     for (int i = 0; i < kWarps * R; ++i) sm100::mbar_init(&bars[i], 1);
@@ -587,6 +591,7 @@ __global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
   const float inv = L > 0.f ? p.v_scale / L : 0.f;
   if (tile.slot < 0) {
     if (row_ok) store_out(o, inv);
+    stamp_end();
     return;
   }
   // Split piece: normalised partial row and its base-2 log-sum-exp.
@@ -600,7 +605,10 @@ __global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
       p.ws_lse[static_cast<int64_t>(tile.slot) * UA_DECODE_ROWS + n] =
           L > 0.f ? M + log2f(L) : -INFINITY;
   }
-  if (p.split_counters == nullptr) return;  // a separate combine kernel merges the pieces
+  if (p.split_counters == nullptr) {  // a separate combine kernel merges the pieces
+    stamp_end();
+    return;
+  }
   // Fused combine: the last piece of a group to finish merges all of them
   // (weights 2^(lse_s - lse*)), then re-arms the group's counter for the next call.
   __shared__ int s_last;
@@ -611,7 +619,10 @@ __global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
     s_last = atomicAdd(&p.split_counters[tile.group], 1) == ns - 1;
   }
   __syncthreads();
-  if (!s_last) return;
+  if (!s_last) {
+    stamp_end();
+    return;
+  }
   __threadfence();
   const ua_combine_group grp = p.groups[tile.group];
   if (row_ok) {
@@ -641,10 +652,11 @@ __global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
     store_out(acc, W > 0.f ? 1.f / W : 0.f);
   }
   if (threadIdx.x == 0) p.split_counters[tile.group] = 0;
+  stamp_end();
 }
 
 template <int D, bool FP8>
-cudaError_t launch_decode_d(const KernelParams& p, cudaStream_t stream) {
+cudaError_t launch_decode_d(const KernelParams& p, cudaStream_t stream, bool after_prefill) {
   CUtensorMap mk, mv;
   const int elt = FP8 ? 1 : 2;
   using PL = PageLayout<D, FP8>;
@@ -659,22 +671,37 @@ cudaError_t launch_decode_d(const KernelParams& p, cudaStream_t stream) {
   static std::atomic<uint64_t> smem_set{0};
   e = set_smem_once(decode_kernel<D, FP8>, Ring<D, FP8>::kAlloc, smem_set);
   if (e != cudaSuccess) return e;
-  decode_kernel<D, FP8><<<p.num_tiles, kThreads, Ring<D, FP8>::kAlloc, stream>>>(mk, mv, p);
-  return cudaGetLastError();
+  if (!after_prefill) {
+    decode_kernel<D, FP8><<<p.num_tiles, kThreads, Ring<D, FP8>::kAlloc, stream>>>(mk, mv, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.num_tiles));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Ring<D, FP8>::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel<D, FP8>, mk, mv, p);
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cudaStream_t stream) {
+cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cudaStream_t stream,
+                          bool after_prefill) {
   if (p.num_tiles <= 0) return cudaSuccess;
+  const bool a = after_prefill;
   if (kv_dtype == UA_KV_BF16) {
-    if (head_dim == 256) return launch_decode_d<256, false>(p, stream);
-    return head_dim == 128 ? launch_decode_d<128, false>(p, stream)
-                           : launch_decode_d<64, false>(p, stream);
+    if (head_dim == 256) return launch_decode_d<256, false>(p, stream, a);
+    return head_dim == 128 ? launch_decode_d<128, false>(p, stream, a)
+                           : launch_decode_d<64, false>(p, stream, a);
   }
-  if (head_dim == 256) return launch_decode_d<256, true>(p, stream);
-  return head_dim == 128 ? launch_decode_d<128, true>(p, stream)
-                         : launch_decode_d<64, true>(p, stream);
+  if (head_dim == 256) return launch_decode_d<256, true>(p, stream, a);
+  return head_dim == 128 ? launch_decode_d<128, true>(p, stream, a)
+                         : launch_decode_d<64, true>(p, stream, a);
 }
 
 }  // namespace ua

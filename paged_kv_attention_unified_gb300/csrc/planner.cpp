@@ -301,10 +301,42 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
                      [&](size_t a, size_t b) { return tail_c[a] > tail_c[b]; });
     s.prefill = std::move(bulk);
     for (size_t k : tail_order) s.prefill.push_back(tail[k]);
+    s.prefill_blocks = total_cost;
     s.prefill_ctas = static_cast<int32_t>(std::min<int64_t>(num_sms, static_cast<int64_t>(n)));
   }
+  {
+    const int elt = p.kv_dtype == UA_KV_FP8_E4M3 ? 1 : 2;
+    int64_t keys = 0;
+    for (const ua_tile& t : s.decode) keys += t.kv_hi - t.kv_lo;
+    s.decode_bytes = keys * 2 * static_cast<int64_t>(p.head_dim) * elt;
+  }
+  if (!s.prefill.empty() && !s.decode.empty())
+    s.prefill_ctas = mixed_prefill_ctas(s.prefill_blocks, s.decode_bytes,
+                                        static_cast<int64_t>(s.prefill.size()), num_sms,
+                                        p.head_dim);
   *out = std::move(s);
   return UA_OK;
+}
+
+int32_t mixed_prefill_ctas(int64_t prefill_blocks, int64_t decode_bytes, int64_t prefill_tiles,
+                           int num_sms, int head_dim) {
+  const int64_t cap = std::min<int64_t>(num_sms, prefill_tiles);
+  if (cap <= 1 || decode_bytes <= 0) return static_cast<int32_t>(std::max<int64_t>(cap, 1));
+  const double work_ns = static_cast<double>(prefill_blocks) * kPrefillBlockNs * head_dim / 128.0;
+  double best_t = 0.0;
+  int64_t best_p = cap;
+  for (int64_t P = 1; P <= cap; ++P) {
+    const double tp = work_ns / static_cast<double>(P);
+    const double bw =
+        std::min(kDecodeHbmBytesPerNs, static_cast<double>(num_sms - P) * kDecodeSmBytesPerNs);
+    const double left = static_cast<double>(decode_bytes) - bw * tp;
+    const double t = left > 0.0 ? tp + left / kDecodeHbmBytesPerNs : tp;
+    if (P == 1 || t < best_t) {
+      best_t = t;
+      best_p = P;
+    }
+  }
+  return static_cast<int32_t>(best_p);
 }
 
 int64_t workspace_bytes(const Schedule& s, int head_dim) {

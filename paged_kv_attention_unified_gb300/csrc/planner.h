@@ -37,7 +37,13 @@ struct Problem {
 struct Schedule {
   // Prefill tiles in the order the persistent prefill CTAs take them.
   std::vector<ua_tile> prefill;
-  int32_t prefill_ctas = 0;  // persistent prefill CTAs: min(SMs, prefill tiles)
+  // Persistent prefill CTAs (one per SM). Without decode work: min(SMs,
+  // prefill tiles). With decode work too, fewer, so that the decode kernel
+  // streams the cache on the other SMs while the prefill runs (see
+  // mixed_prefill_ctas).
+  int32_t prefill_ctas = 0;
+  int64_t prefill_blocks = 0;   // prefill work in 128 x 128 (query row, key) blocks
+  int64_t decode_bytes = 0;     // K/V bytes the decode tiles read
   std::vector<ua_tile> decode;
   // fp8 caches: the keys and values the prefill tiles read are first widened
   // to bf16 into a staging cache of kStagePage-slot pages (a sequence's pages
@@ -87,6 +93,20 @@ constexpr int kAppendTokens = 8;
 // Share of the prefill work (in 128 x 128 query-key blocks) kept for the end
 // of the prefill list: the shortest tiles, so that the CTAs finish together.
 constexpr double kPrefillTailShare = 1.0 / 16.0;
+
+// Mixed batches: the prefill kernel takes one whole SM per CTA (its shared
+// memory excludes decode CTAs there), the decode kernel the SMs it leaves.
+// With P prefill CTAs the prefill part takes about blocks * t_block / P, the
+// decode part streams at min(HBM, (SMs - P) * per-SM rate) meanwhile and at
+// the full HBM rate once the prefill SMs free up; P minimises the modelled
+// step time. Constants measured on GB300 (bf16, head_dim 128): one 128 x 128
+// block of one query tile costs about 1.3 us of one SM; decode streams about
+// 6.5 bytes/ns from HBM in all and at most kDecodeSmBytesPerNs per SM.
+constexpr double kPrefillBlockNs = 1300.0;
+constexpr double kDecodeHbmBytesPerNs = 6500.0;
+constexpr double kDecodeSmBytesPerNs = 90.0;
+int32_t mixed_prefill_ctas(int64_t prefill_blocks, int64_t decode_bytes, int64_t prefill_tiles,
+                           int num_sms, int head_dim);
 
 // Validate the problem (host arrays included).
 ua_status validate(const Problem& p);

@@ -689,6 +689,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
+  // A decode grid queued behind this one with programmatic stream
+  // serialization may start once every prefill CTA has started: it then
+  // takes the SMs these CTAs leave free. It reads nothing this grid writes.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0 && p.span_start != nullptr) atomicMin(p.span_start, globaltimer_ns());
+
   if (tid == 0) {
     *abort = 0;
     *never = 0;
@@ -745,6 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (tid == 0 && p.span_end != nullptr) atomicMax(p.span_end, globaltimer_ns());
 }
 
 template <int D>

@@ -3,6 +3,7 @@
 // launches of one forward call.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstring>
@@ -31,11 +32,6 @@ struct ua_plan {
   ua_tile* d_stage = nullptr;             // fp8 prefill: stage tiles
   void* d_staged_k = nullptr;             // fp8 prefill: bf16 staging caches
   void* d_staged_v = nullptr;
-  // A batch with both prefill and decode tiles runs the two kernels on two
-  // streams (the caller's and a side stream from the library's pool), forked
-  // and joined with events, so that each fills the SMs the other leaves.
-  cudaStream_t side = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   float* d_ws = nullptr;           // split workspace: partial rows then lse values
   float* d_ws_o = nullptr;
   float* d_ws_lse = nullptr;
@@ -45,6 +41,7 @@ struct ua_plan {
   bool unified_max_on = false;     // ua_plan_set_unified_max
   float unified_max = 0.f;
   uint64_t wait_timeout_ns = 2000000000ull;
+  int32_t prefill_ctas_override = 0;  // ua_plan_set_prefill_ctas (0: the scheduler's count)
   // kernel timing (ua_plan_set_profiling)
   struct EventPair {
     cudaEvent_t start = nullptr, stop = nullptr;
@@ -52,6 +49,12 @@ struct ua_plan {
   };
   bool profiling = false;
   std::vector<EventPair> ev_pending, ev_free;
+  // The prefill and decode kernels time themselves (first CTA start, last CTA
+  // end on the device global timer) into slot i of these arrays: an event
+  // recorded between the two launches of a mixed batch would stop the decode
+  // grid from starting while the prefill grid runs.
+  unsigned long long* d_span = nullptr;  // [kSpanSlots] starts, then [kSpanSlots] ends
+  std::vector<std::pair<int, int>> span_pending;  // (kind, slot)
 };
 
 namespace {
@@ -134,32 +137,7 @@ void pinned_give_back(const PinnedBlock& b) {
   g_pinned_free.push_back(b);
 }
 
-// Side streams for the decode half of a mixed forward, reused across plans
-// (creating a stream per plan would cost every mixed serving step): a plan
-// takes one on its first mixed forward and returns it when destroyed; work
-// still queued on it is unaffected (the next user queues behind it).
-std::mutex g_side_mu;
-std::vector<std::pair<int, cudaStream_t>> g_side_free;
-
-cudaStream_t side_take(int device) {
-  {
-    std::lock_guard<std::mutex> lock(g_side_mu);
-    for (size_t i = 0; i < g_side_free.size(); ++i)
-      if (g_side_free[i].first == device) {
-        cudaStream_t st = g_side_free[i].second;
-        g_side_free.erase(g_side_free.begin() + static_cast<std::ptrdiff_t>(i));
-        return st;
-      }
-  }
-  cudaStream_t st = nullptr;
-  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-  return st;
-}
-
-void side_give_back(int device, cudaStream_t st) {
-  std::lock_guard<std::mutex> lock(g_side_mu);
-  g_side_free.emplace_back(device, st);
-}
+constexpr int kSpanSlots = 1024;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -173,11 +151,8 @@ void free_plan_memory(ua_plan* p) {
   p->ev_free.clear();
   // stream-ordered: the memory returns to the pool once the plan's last
   // stream has finished with it
-  if (p->side) side_give_back(p->device, p->side);
-  if (p->ev_fork) cudaEventDestroy(p->ev_fork);
-  if (p->ev_join) cudaEventDestroy(p->ev_join);
-  p->side = nullptr;
-  p->ev_fork = p->ev_join = nullptr;
+  if (p->d_span) cudaFreeAsync(p->d_span, p->last_stream);
+  p->d_span = nullptr;
   if (p->d_meta) cudaFreeAsync(p->d_meta, p->last_stream);
   if (p->d_ws) cudaFreeAsync(p->d_ws, p->last_stream);
   if (p->d_staged_k) cudaFreeAsync(p->d_staged_k, p->last_stream);
@@ -279,6 +254,27 @@ ua_plan::EventPair* timing_begin(ua_plan* p, int kind, cudaStream_t cs) {
 
 void timing_end(ua_plan::EventPair* e, cudaStream_t cs) {
   if (e) cudaEventRecord(e->stop, cs);
+}
+
+// Span slot for a self-timed launch of `kind` (prefill 0, decode 1): the
+// kernel's start / end words, or nulls when not profiling or out of slots.
+void span_begin(ua_plan* p, int kind, unsigned long long** start, unsigned long long** end) {
+  *start = *end = nullptr;
+  if (!p->profiling || p->d_span == nullptr) return;
+  const int slot = static_cast<int>(p->span_pending.size());
+  if (slot >= kSpanSlots) return;
+  p->span_pending.emplace_back(kind, slot);
+  *start = p->d_span + slot;
+  *end = p->d_span + kSpanSlots + slot;
+}
+
+// Span words back to "empty": starts at the largest value, ends at zero.
+cudaError_t span_reset(ua_plan* p, int slots, cudaStream_t cs) {
+  if (slots <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(p->d_span, 0xFF, slots * sizeof(unsigned long long), cs);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(p->d_span + kSpanSlots, 0, slots * sizeof(unsigned long long), cs);
+  return e;
 }
 
 }  // namespace
@@ -504,6 +500,7 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
   mp->last_stream = cs;
   ua::KernelParams kp = base_params(plan, q, k_cache, v_cache, out, cu_query_lens, kv_lens,
                                     block_tables, num_blocks, scale, k_scale, v_scale);
+  const bool mixed = !s.prefill.empty() && !s.decode.empty();
   auto run_prefill = [&](cudaStream_t cs) -> ua_status {
     const bool staged = plan->prob.prefill_staged;
     const void* pk = k_cache;
@@ -535,7 +532,11 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     pp.tiles = plan->d_prefill;
     pp.num_tiles = static_cast<int32_t>(s.prefill.size());
     pp.counters = plan->d_prefill_counters;
-    pp.num_ctas = plan->info.num_prefill_ctas;
+    pp.num_ctas = plan->prefill_ctas_override > 0
+                      ? std::min<int32_t>(plan->prefill_ctas_override,
+                                          std::min<int32_t>(plan->info.num_sms,
+                                                            static_cast<int32_t>(s.prefill.size())))
+                      : plan->info.num_prefill_ctas;
     pp.cu_query_lens = cu_query_lens;
     pp.kv_lens = kv_lens;
     pp.block_tables = staged ? plan->d_staged_table : block_tables;
@@ -553,47 +554,46 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     pp.rows_per_box = pp.block_size < 128 ? pp.block_size : 128;
     pp.timeout_ns = plan->wait_timeout_ns;
     pp.debug_flags = plan->debug_flags;
-    auto* ev = timing_begin(mp, 0, cs);
+    // Timing: CUDA events around a kernel that runs alone; in a mixed batch
+    // the kernels time themselves (an event between the two launches would
+    // hold the decode grid back until the prefill grid ends).
+    ua_plan::EventPair* ev = nullptr;
+    if (mixed) span_begin(mp, 0, &pp.span_start, &pp.span_end);
+    else ev = timing_begin(mp, 0, cs);
     if (ua::launch_prefill(pp, q, pk, pv, plan->total_q, plan->prob.head_dim,
                            plan->prob.num_kv_heads, cs) != cudaSuccess)
       return UA_ERR_CUDA;
     timing_end(ev, cs);
     return UA_OK;
   };
-  auto run_decode = [&](cudaStream_t cs) -> ua_status {
+  auto run_decode = [&](cudaStream_t cs, bool after_prefill) -> ua_status {
     kp.tiles = plan->d_decode;
     kp.num_tiles = static_cast<int32_t>(s.decode.size());
     // split pieces are merged inside the decode launch (last piece per group)
     kp.split_counters = s.groups.empty() ? nullptr : plan->d_counters;
     kp.groups = plan->d_groups;
-    auto* ev = timing_begin(mp, 1, cs);
-    if (ua::launch_decode(kp, plan->prob.head_dim, plan->prob.kv_dtype, cs) != cudaSuccess)
+    ua_plan::EventPair* ev = nullptr;
+    if (mixed) span_begin(mp, 1, &kp.span_start, &kp.span_end);
+    else ev = timing_begin(mp, 1, cs);
+    if (ua::launch_decode(kp, plan->prob.head_dim, plan->prob.kv_dtype, cs, after_prefill) !=
+        cudaSuccess)
       return UA_ERR_CUDA;
     timing_end(ev, cs);
     return UA_OK;
   };
-  if (!s.prefill.empty() && !s.decode.empty()) {
-    if (mp->side == nullptr) {
-      mp->side = side_take(plan->device);
-      if (mp->side == nullptr ||
-          cudaEventCreateWithFlags(&mp->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-          cudaEventCreateWithFlags(&mp->ev_join, cudaEventDisableTiming) != cudaSuccess)
-        return UA_ERR_CUDA;
-    }
-    // fork: the decode half waits for everything queued on the caller's
-    // stream; join: the caller's stream waits for the decode half
-    if (cudaEventRecord(mp->ev_fork, cs) != cudaSuccess ||
-        cudaStreamWaitEvent(mp->side, mp->ev_fork, 0) != cudaSuccess)
-      return UA_ERR_CUDA;
+  if (mixed) {
+    // Mixed batch, one stream: every prefill CTA signals at its start that a
+    // grid queued behind it with programmatic serialization may launch, so
+    // the decode grid starts while the prefill runs -- its CTAs take the SMs
+    // the num_prefill_ctas prefill CTAs leave, then the prefill SMs as those
+    // CTAs finish. The two grids write disjoint outputs and share only
+    // read-only inputs; work queued on `stream` afterwards waits for both.
     const ua_status st_pre = run_prefill(cs);
-    const ua_status st_dec = run_decode(mp->side);
-    if (cudaEventRecord(mp->ev_join, mp->side) != cudaSuccess ||
-        cudaStreamWaitEvent(cs, mp->ev_join, 0) != cudaSuccess)
-      return UA_ERR_CUDA;
-    return st_pre != UA_OK ? st_pre : st_dec;
+    if (st_pre != UA_OK) return st_pre;
+    return run_decode(cs, true);
   }
   if (!s.prefill.empty()) return run_prefill(cs);
-  if (!s.decode.empty()) return run_decode(cs);
+  if (!s.decode.empty()) return run_decode(cs, false);
   return UA_OK;
 }
 
@@ -713,6 +713,14 @@ ua_status ua_gather_kv_debug(const ua_plan* plan, const void* k_cache, const voi
 
 ua_status ua_plan_set_profiling(ua_plan* plan, int32_t enable) {
   if (plan == nullptr) return UA_ERR_INVALID_ARG;
+  if (enable && plan->d_span == nullptr) {
+    void* ptr = nullptr;
+    if (plan_alloc(&ptr, 2 * kSpanSlots * sizeof(unsigned long long), plan->device,
+                   plan->last_stream) != cudaSuccess)
+      return UA_ERR_CUDA;
+    plan->d_span = static_cast<unsigned long long*>(ptr);
+    if (span_reset(plan, kSpanSlots, plan->last_stream) != cudaSuccess) return UA_ERR_CUDA;
+  }
   plan->profiling = enable != 0;
   return UA_OK;
 }
@@ -733,6 +741,22 @@ ua_status ua_plan_kernel_times(ua_plan* plan, float* ms, int64_t* launches) {
     plan->ev_free.push_back(e);
   }
   plan->ev_pending.clear();
+  const int used = static_cast<int>(plan->span_pending.size());
+  if (used > 0) {
+    std::vector<unsigned long long> t(2 * kSpanSlots);
+    if (cudaMemcpy(t.data(), plan->d_span, 2 * kSpanSlots * sizeof(unsigned long long),
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+      return UA_ERR_CUDA;
+    for (const auto& ks : plan->span_pending) {
+      const unsigned long long t0 = t[ks.second], t1 = t[kSpanSlots + ks.second];
+      if (t1 >= t0) ms[ks.first] += static_cast<float>(static_cast<double>(t1 - t0) * 1e-6);
+      launches[ks.first] += 1;
+    }
+    plan->span_pending.clear();
+    if (span_reset(plan, used, plan->last_stream) != cudaSuccess ||
+        cudaStreamSynchronize(plan->last_stream) != cudaSuccess)
+      st = UA_ERR_CUDA;
+  }
   return st;
 }
 
@@ -741,6 +765,12 @@ ua_status ua_plan_set_debug(ua_plan* plan, int32_t flags, int64_t wait_timeout_n
   plan->debug_flags = flags;
   plan->wait_timeout_ns = wait_timeout_ns > 0 ? static_cast<uint64_t>(wait_timeout_ns)
                                               : 2000000000ull;
+  return UA_OK;
+}
+
+ua_status ua_plan_set_prefill_ctas(ua_plan* plan, int32_t num_ctas) {
+  if (plan == nullptr || num_ctas < 0) return UA_ERR_INVALID_ARG;
+  plan->prefill_ctas_override = num_ctas;
   return UA_OK;
 }
 

@@ -47,6 +47,10 @@ struct KernelParams {
   // decode row, in log2 units of the scaled score (phi * log2(e)).
   int32_t unified_max_on;
   float unified_max_log2;
+  // Kernel timing (null: off): first CTA start (atomicMin) and last CTA end
+  // (atomicMax) on the device global timer, in ns.
+  unsigned long long* span_start;
+  unsigned long long* span_end;
 };
 
 struct CombineParams {

@@ -48,6 +48,10 @@ struct PrefillParams {
   int32_t rows_per_box;     // keys per TMA box: min(block_size, 128)
   uint64_t timeout_ns;      // bound of every mbarrier wait
   int32_t debug_flags;      // bit 0: the producer issues nothing (timeout test)
+  // Kernel timing (null: off): the first CTA's start (atomicMin) and the last
+  // CTA's end (atomicMax) on the device global timer, in ns.
+  unsigned long long* span_start;
+  unsigned long long* span_end;
 };
 
 // Bit 0 of PrefillParams::debug_flags: the TMA producer skips every load, so
@@ -59,7 +63,9 @@ constexpr int32_t kDebugProducerIdle = 1;
 bool prefill_supported(int head_dim, int kv_dtype, int qpk, int block_size);
 
 // Persistent prefill kernel: p.num_ctas CTAs take p.tiles in order as they
-// free up (the host encodes the tensor maps from the pointers).
+// free up (the host encodes the tensor maps from the pointers). Every CTA
+// allows a grid queued behind it with programmatic stream serialization to
+// start once all of them have started.
 cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_cache,
                            const void* v_cache, int64_t total_q, int head_dim,
                            int num_kv_heads, cudaStream_t stream);
@@ -78,8 +84,12 @@ cudaError_t encode_kv_page_map(CUtensorMap* map, const void* cache, int elt_byte
                                int num_kv_heads, int block_size, int64_t num_blocks,
                                int box_dims, int box_rows, bool swizzle_128b);
 
-// Split-KV decode kernel over p.tiles[0 .. p.num_tiles).
-cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cudaStream_t stream);
+// Split-KV decode kernel over p.tiles[0 .. p.num_tiles). after_prefill: the
+// launch directly follows a prefill launch on `stream` and may start as soon
+// as every prefill CTA has started (programmatic stream serialization; the
+// two grids touch disjoint outputs and share only read-only inputs).
+cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cudaStream_t stream,
+                          bool after_prefill = false);
 
 // Log-sum-exp combine of split partials into bf16 output rows.
 cudaError_t launch_combine(const CombineParams& c, int head_dim, cudaStream_t stream);

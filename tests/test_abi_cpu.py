@@ -266,7 +266,31 @@ def test_prefill_list_ends_with_shortest_tiles(case):
             assert key not in seen
             seen.add(key)
             prev = key
-    assert info.num_prefill_ctas == min(152, len(pre))
+    if case == "dense":
+        assert info.num_prefill_ctas == min(152, len(pre))
+    else:   # mixed: some SMs are left to the decode kernel
+        assert 1 <= info.num_prefill_ctas < min(152, len(pre))
+
+
+def _mixed_ctas(n_prefill_seqs, prefill_q, n_decode, decode_kv):
+    ql = [prefill_q] * n_prefill_seqs + [1] * n_decode
+    kv = [prefill_q] * n_prefill_seqs + [decode_kv] * n_decode
+    cu = [0] + [int(x) for x in np.cumsum(ql)]
+    info, pre, dec, _ = ua.ua_schedule(cu, kv, 32, 8, 128, 16, max(kv) // 16 + 1)
+    return info.num_prefill_ctas, len(pre)
+
+
+def test_mixed_prefill_cta_count_follows_the_work_balance():
+    """With decode work in the batch the prefill kernel gets fewer SMs: more as
+    its share of the work grows, all of them (up to its tile count) when there
+    is no decode work, and at least one."""
+    alone, tiles = _mixed_ctas(4, 2048, 0, 0)
+    assert alone == min(152, tiles)
+    counts = [_mixed_ctas(4, 2048, nd, 8192)[0] for nd in (8, 64, 256, 1024)]
+    assert all(a >= b for a, b in zip(counts, counts[1:])), counts   # more decode -> fewer
+    assert counts[-1] >= 1 and counts[0] <= 152
+    grow = [_mixed_ctas(ns, 2048, 128, 4096)[0] for ns in (1, 4, 16)]
+    assert all(a <= b for a, b in zip(grow, grow[1:])), grow       # more prefill -> more
 
 
 def _piece_lengths(dec):
