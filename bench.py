@@ -45,8 +45,10 @@ WORKLOAD_NAMES = {
        "configuration: measures split sizing on equal lengths)",
     8: "pure decode at head_dim 256: 64 seqs, q 1, kv U[512,4096], 32/8 heads, bf16, bs16 "
        "(not a benchmark configuration: measures the head_dim 256 decode path)",
+    9: "dense causal prefill at head_dim 256: 4 seqs x 4096, 32/32 heads, bf16, bs128, identity "
+       "table (not a benchmark configuration: measures the head_dim 256 prefill kernel)",
 }
-FLOP_CONFIGS = (4, 6)   # prefill-bound workloads, reported in TFLOP/s
+FLOP_CONFIGS = (4, 6, 9)   # prefill-bound workloads, reported in TFLOP/s
 
 
 def _seq_work(case):
@@ -389,22 +391,27 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
         per_step_ms = max(1e-3, _timed_steps(1, step, stream, flush))
         chunk = max(1, int(100.0 / per_step_ms))
         soak_ms, soak_n = 0.0, 0
-        while soak_ms < soak_s * 1e3 or soak_n < args.steps:
+        while soak_s > 0 and (soak_ms < soak_s * 1e3 or soak_n < args.steps):
             soak_ms += _timed_steps(chunk, step, stream, flush)
             soak_n += chunk
-        ua.ua_plan_set_profiling(plan.handle, True)
-        ua.ua_plan_kernel_times(plan.handle)      # synchronises; nothing recorded yet
+        # the K timed steps: nothing but the forward in the stream
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         ms = _timed_steps(args.steps, step, stream, flush)
         if world > 1:
             dist.barrier()
+        # K more steps with the library's per-kernel timing on (an event pair
+        # around each lone kernel costs a few microseconds of step time, so it
+        # stays out of the K steps above)
+        ua.ua_plan_set_profiling(plan.handle, True)
+        ua.ua_plan_kernel_times(plan.handle)      # synchronises; nothing recorded yet
+        _timed_steps(args.steps, step, stream, flush)
+        ktimes = ua.ua_plan_kernel_times(plan.handle)
+        ua.ua_plan_set_profiling(plan.handle, False)
         clk.end_load()
-    ktimes = ua.ua_plan_kernel_times(plan.handle)
-    ua.ua_plan_set_profiling(plan.handle, False)
     ms_max = max_over_ranks(ms, world, device="cuda")
-    soak_max = max_over_ranks(soak_ms / soak_n, world, device="cuda")
+    soak_max = max_over_ranks(soak_ms / max(soak_n, 1), world, device="cuda")
     step_s = ms_max / 1e3 / args.steps
     job_bytes = sum_over_ranks(byts, world, device="cuda")
     job_flops = sum_over_ranks(flops, world, device="cuda")
@@ -445,8 +452,8 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
         r["kernel_avg_us"] = avg_s * 1e6
         r["kernel_share"] = kms / max(1e-9, sum(v[0] for v in ktimes.values()))
         r["timing"] = ("device global-timer span, first CTA start to last CTA end (the two "
-                       "kernels of a mixed step overlap)") if mixed else \
-            "CUDA events on the launching stream"
+                       "kernels of a mixed step overlap), over K steps after the timed ones") \
+            if mixed else "CUDA events on the launching stream, over K steps after the timed ones"
         traffic, note, digests = _traffic_record(kind, cfg)
         r["traffic"] = traffic
         if note:
@@ -463,18 +470,20 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
         roof["other_kernels"] = {k: v for k, v in rooflines.items() if k != kind}
     launches = sum(v[1] for v in ktimes.values())
 
-    # end to end through the public API with host buffers, plan included
+    # end to end through the public API with host buffers: one ua_forward_host
+    # call per step (scheduling, upload of tiles + lengths + page tables, H2D
+    # of q, forward, D2H of the output, synchronisation)
     e2e = None
     if not args.no_e2e:
-        q_h = case.q.pin_memory()
+        q_h = case.q.contiguous().pin_memory()
         cu_h = case.cu_query_lens.to(torch.int32).pin_memory()
         kv_h = case.kv_lens.to(torch.int32).pin_memory()
-        bt_h = case.block_tables.to(torch.int32).pin_memory()
+        bt_h = case.block_tables.to(torch.int32).contiguous().pin_memory()
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         tiles_b = 32 * (info.num_prefill_tiles + info.num_decode_tiles) + \
             32 * info.num_combine_groups + 16
         h2d = q_h.numel() * 2 + cu_h.numel() * 4 + kv_h.numel() * 4 + bt_h.numel() * 4 + tiles_b
-        d2h = out_h.numel() * 2
+        d2h = out_h.numel() * 2 + 4
         torch.cuda.synchronize()
         tot = 0.0
         for it in range(args.warmup + args.steps):
@@ -482,24 +491,22 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
                 flush.zero_()
                 torch.cuda.synchronize()
             t_0 = time.perf_counter()
-            b.q.copy_(q_h, non_blocking=True)
-            b.cu_query_lens.copy_(cu_h, non_blocking=True)
-            b.kv_lens.copy_(kv_h, non_blocking=True)
-            b.block_tables.copy_(bt_h, non_blocking=True)
-            with tu.make_plan(b, num_splits=args.num_splits) as p2:
-                p2.set_unified_max(args.unified_max)
-                if args.prefill_ctas:
-                    ua.ua_plan_set_prefill_ctas(p2.handle, args.prefill_ctas)
-                tu.forward(p2, b, out)
-                out_h.copy_(out, non_blocking=True)
-                torch.cuda.synchronize()
+            err = ua.ua_forward_host(q_h, out_h, cu_h, kv_h, bt_h, b.k_cache, b.v_cache,
+                                     b.num_q_heads, b.num_kv_heads, b.head_dim, b.block_size,
+                                     b.num_blocks, b.kv_dtype, b.scale, causal=b.causal,
+                                     window=b.window, k_scale=b.k_scale, v_scale=b.v_scale,
+                                     num_splits=args.num_splits)
             if it >= args.warmup:
                 tot += time.perf_counter() - t_0
+            assert err == 0, f"device error word {err}"
         e2e_s = max_over_ranks(tot / args.steps, world, device="cuda")
         e2e = {"value": _rate(cfg, job_bytes, job_flops, e2e_s), "unit": _metric_for(cfg)[1],
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "includes": "H2D of q/lengths/page tables, CPU scheduling + tile upload, "
-                           "forward, D2H of the output, per step"}
+               "includes": "one ua_forward_host call per step: CPU scheduling, one upload of "
+                           "tiles + lengths + page tables, H2D of q, forward, D2H of the output "
+                           "and the error word, stream synchronisation (pinned host buffers)"}
+        if args.unified_max is not None or args.prefill_ctas:
+            e2e["note"] = "the scheduler's default settings (no unified max / CTA override)"
     plan.close()
     l2_note = ("inputs larger than L2 (%.2f GB > 0.129 GB)" % (byts / 1e9)) if flush is None \
         else "L2 flushed (256 MB write) between timed steps"
@@ -509,7 +516,8 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
         "workload": WORKLOAD_NAMES[cfg], "metric": _metric_for(cfg)[0], "value": value,
         "unit": _metric_for(cfg)[1], "steps": args.steps, "ms_per_step": ms_max / args.steps,
         "sustained": {"value": _rate(cfg, job_bytes, job_flops, soak_max / 1e3),
-                      "ms_per_step": soak_max, "steps": soak_n, "seconds": soak_ms / 1e3},
+                      "ms_per_step": soak_max, "steps": soak_n, "seconds": soak_ms / 1e3}
+        if soak_n else None,
         "dtype": _dtype_for(case),
         "l2": l2_note,
         "tiles": {"decode": info.num_decode_tiles, "prefill": info.num_prefill_tiles,

@@ -41,9 +41,11 @@
  * the "Fused Attention" notes). It replaces the per-program binary search over
  * the query prefix sums that the vLLM kernel performs at run time.
  *
- * Supported: head_dim 64, 128 (prefill and decode kernels) and 256 (decode
- * kernel for every sequence); block_size a multiple of 16; any GQA ratio
- * (the prefill kernel takes ratios dividing 128, other ratios run in the
+ * Supported: head_dim 64, 128 and 256, each with a prefill and a decode
+ * kernel (the head_dim 256 prefill kernel works on one 128-row query tile and
+ * 64-key tiles at a time and takes block sizes that 64 divides or that
+ * divide 64); block_size a multiple of 16; any GQA ratio (the prefill
+ * kernels take ratios dividing 128; sequences they cannot take run in the
  * decode kernel).
  *
  * Conventions.
@@ -56,7 +58,7 @@
  *  - All device work is ordered on the stream argument (a mixed batch's
  *    decode half runs on a side stream forked from and joined back into it);
  *    nothing synchronises the host except ua_last_device_error,
- *    ua_plan_kernel_times and ua_forward_oneshot.
+ *    ua_plan_kernel_times, ua_forward_oneshot and ua_forward_host.
  *  - No entry point calls exit, abort or a device trap. Invalid arguments are
  *    rejected with a negative status before anything is launched.
  */
@@ -141,9 +143,10 @@ typedef struct ua_plan ua_plan;
  * decode tile's key range into min(n, ceil(len/16)) pieces; at most
  * UA_MAX_SPLITS. num_sms <= 0 means 152.
  * decode_rows_max: sequences with q_len * qpk <= this value go to the decode
- * kernel, the others to the prefill kernel (when it takes the problem: head
- * dim 64 or 128, 128 % qpk == 0, and a bf16 cache with block_size and 128
- * dividing one another or any fp8 cache); < 0 means the built-in default (32).
+ * kernel, the others to a prefill kernel (when one takes the problem:
+ * 128 % qpk == 0, and a bf16 cache whose block_size and the key tile (128
+ * keys at head dim 64 / 128, 64 at head dim 256) divide one another, or any
+ * fp8 cache); < 0 means the built-in default (32).
  * The prefill list is in the order the persistent prefill CTAs take it
  * (grouped by sequence and KV head, the shortest tiles last); the decode list
  * is longest first.
@@ -238,6 +241,35 @@ ua_status ua_forward_oneshot(const void* q, const void* k_cache, const void* v_c
                              int32_t max_kv, float scale, int32_t causal, int32_t window,
                              float k_scale, float v_scale, int32_t num_splits,
                              ua_stream_t stream);
+
+/*
+ * ua_forward_host -- one serving step from host buffers: the whole of
+ * ua_forward_oneshot, with the queries, output, lengths and page tables in
+ * host memory and the paged K/V cache resident on the device. Schedules the
+ * batch, uploads the tile list together with the lengths and page tables in
+ * one copy, copies q to the device, runs the forward, copies the output
+ * back, and synchronises `stream` before returning.
+ * q_host, out_host: [total_q, num_q_heads, head_dim] bf16 in host memory
+ *   (page-locked memory, e.g. cudaHostAlloc, gives asynchronous copies;
+ *   pageable memory works, its copies synchronise).
+ * cu_query_lens_host [num_seqs+1], kv_lens_host [num_seqs],
+ * block_tables_host [num_seqs, max_blocks_per_seq]: host int32, as for
+ *   ua_forward.
+ * k_cache, v_cache: device caches, as for ua_forward.
+ * error_word: optional host int32 that receives the call's device error
+ *   word (UA_OK, UA_ERR_BOUNDS or UA_ERR_DEVICE_TIMEOUT); may be NULL.
+ * Device memory for the plan, q and the output comes from the library's
+ * stream-ordered pool and is returned to it before the call returns.
+ * Returns as ua_plan_create and ua_forward.
+ */
+ua_status ua_forward_host(const void* q_host, void* out_host, const int32_t* cu_query_lens_host,
+                          const int32_t* kv_lens_host, const int32_t* block_tables_host,
+                          const void* k_cache, const void* v_cache, int32_t num_seqs,
+                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks,
+                          int32_t kv_dtype, float scale, int32_t causal, int32_t window,
+                          float k_scale, float v_scale, int32_t num_splits,
+                          int32_t* error_word, ua_stream_t stream);
 
 /*
  * ua_append_kv -- write a step's new keys and values into the paged cache

@@ -34,7 +34,7 @@ EXPORTS = (
     "ua_plan_get_info", "ua_last_device_error", "ua_plan_destroy", "ua_status_string",
     "ua_gather_kv_debug", "ua_plan_set_profiling", "ua_plan_kernel_times",
     "ua_forward_static_scratch", "ua_plan_set_debug", "ua_append_kv",
-    "ua_plan_set_unified_max", "ua_plan_set_prefill_ctas",
+    "ua_plan_set_unified_max", "ua_plan_set_prefill_ctas", "ua_forward_host",
 )
 
 
@@ -85,6 +85,8 @@ _SIGS = {
     "ua_forward_oneshot": (_I32, [_P, _P, _P, _P, _I32P, _I32P, _P, _P, _P, _I32, _I32, _I32,
                                   _I32, _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32, _I32, _F,
                                   _F, _I32, _P]),
+    "ua_forward_host": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
+                               _I32, _I64, _I32, _F, _I32, _I32, _F, _F, _I32, _I32P, _P]),
     "ua_plan_get_info": (_I32, [_P, ctypes.POINTER(ua_plan_info)]),
     "ua_last_device_error": (_I32, [_P, _I32P]),
     "ua_plan_destroy": (_I32, [_P]),
@@ -219,6 +221,26 @@ def ua_forward_oneshot(q, k_cache, v_cache, out, cu_query_lens_host, kv_lens_hos
                                     int(max_kv), float(scale), causal, window, float(k_scale),
                                     float(v_scale), num_splits, _stream_handle(stream)),
            "ua_forward_oneshot")
+
+
+def ua_forward_host(q_host, out_host, cu_query_lens_host, kv_lens_host, block_tables_host,
+                    k_cache, v_cache, num_q_heads, num_kv_heads, head_dim, block_size,
+                    num_blocks, kv_dtype, scale, causal=1, window=0, k_scale=1.0, v_scale=1.0,
+                    num_splits=0, stream=None) -> int:
+    """One step from host buffers (q/out/lengths/page tables on the host, the
+    cache on the device); returns the device error word. Host tensors:
+    contiguous CPU tensors (bf16 q / out, int32 lengths and page tables),
+    pinned for asynchronous copies."""
+    n = int(kv_lens_host.shape[0])
+    err = ctypes.c_int32(0)
+    _check(lib().ua_forward_host(
+        q_host.data_ptr(), out_host.data_ptr(), cu_query_lens_host.data_ptr(),
+        kv_lens_host.data_ptr(), block_tables_host.data_ptr(), k_cache.data_ptr(),
+        v_cache.data_ptr(), n, num_q_heads, num_kv_heads, head_dim, block_size,
+        int(block_tables_host.shape[1]) if n else 0, num_blocks, kv_dtype, scale, causal, window,
+        k_scale, v_scale, num_splits, ctypes.byref(err), _stream_handle(stream)),
+        "ua_forward_host")
+    return err.value
 
 
 def ua_last_device_error(plan: int) -> int:

@@ -203,8 +203,10 @@ __device__ __forceinline__ void compute_step(WarpState<D>& st, StepRegs<D, FP8>&
                                              const uint32_t (&qb)[D / 16][2], const float (&cc)[2],
                                              const StepMask& mk, int base, int g, int t) {
   using C = DecodeCfg<D, FP8>;
-  // S^T = K Q^T for the 16 keys of this step.
-  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  // S^T = K Q^T for the 16 keys of this step, in two independent accumulation
+  // chains (even and odd head-dim chunks) that are added at the end: half the
+  // dependent MMA latency per step.
+  float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
   for (int c = 0; c < C::NC; ++c) {
     uint32_t a[4];
@@ -217,13 +219,13 @@ __device__ __forceinline__ void compute_step(WarpState<D>& st, StepRegs<D, FP8>&
       a[2] = r.k[0][2 * c + 1];
       a[3] = r.k[1][2 * c + 1];
     }
-    mma16816<FP8>(s, a, qb[c][0], qb[c][1]);
+    mma16816<FP8>(s[c & 1], a, qb[c][0], qb[c][1]);
   }
   float x[4];
-  x[0] = s[0] * cc[0];
-  x[1] = s[1] * cc[1];
-  x[2] = s[2] * cc[0];
-  x[3] = s[3] * cc[1];
+  x[0] = (s[0][0] + s[1][0]) * cc[0];
+  x[1] = (s[0][1] + s[1][1]) * cc[1];
+  x[2] = (s[0][2] + s[1][2]) * cc[0];
+  x[3] = (s[0][3] + s[1][3]) * cc[1];
   // Masking (a select, so that nothing read from outside the visible set can
   // reach the result) only on steps that straddle a bound.
   if (base < mk.lo_full || base + 16 > mk.hi_full) {

@@ -53,6 +53,34 @@ int64_t wave_fit_chunk(int64_t tiles, int64_t len, int64_t slots) {
   return best_size;
 }
 
+// Indices 0..n-1 ordered by the keys (a, b, c) ascending, ties by index: a
+// stable sort on precomputed keys (the lists are generated in (sequence, KV
+// head, row, key) order, so the index is the documented final tie-break).
+struct SortKey {
+  int64_t a, b, c;
+  int32_t idx;
+};
+
+std::vector<int32_t> order_by(std::vector<SortKey>& keys) {
+  std::sort(keys.begin(), keys.end(), [](const SortKey& x, const SortKey& y) {
+    if (x.a != y.a) return x.a < y.a;
+    if (x.b != y.b) return x.b < y.b;
+    if (x.c != y.c) return x.c < y.c;
+    return x.idx < y.idx;
+  });
+  std::vector<int32_t> order(keys.size());
+  for (size_t i = 0; i < keys.size(); ++i) order[i] = keys[i].idx;
+  return order;
+}
+
+template <typename T>
+void permute(std::vector<T>& v, const std::vector<int32_t>& order) {
+  std::vector<T> out;
+  out.reserve(v.size());
+  for (int32_t i : order) out.push_back(v[static_cast<size_t>(i)]);
+  v.swap(out);
+}
+
 }  // namespace
 
 ua_status validate(const Problem& p) {
@@ -94,6 +122,19 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
 
   // 1. Whole decode tiles (before splitting) and prefill tiles.
   std::vector<ua_tile> dec;
+  {
+    int64_t n_dec = 0, n_pre = 0, n_app = 0;
+    for (int32_t q = 0; q < p.num_seqs; ++q) {
+      const int64_t ql = p.cu_query_lens[q + 1] - p.cu_query_lens[q];
+      const int64_t rows = ql * qpk;
+      if (rows <= rows_max) n_dec += ceil_div(rows, UA_DECODE_ROWS) * p.num_kv_heads;
+      else n_pre += ceil_div(rows, UA_PREFILL_ROWS) * p.num_kv_heads;
+      n_app += ceil_div(ql, kAppendTokens);
+    }
+    dec.reserve(static_cast<size_t>(n_dec));
+    s.prefill.reserve(static_cast<size_t>(n_pre));
+    s.append.reserve(static_cast<size_t>(n_app));
+  }
   for (int32_t q = 0; q < p.num_seqs; ++q) {
     const int32_t ql = p.cu_query_lens[q + 1] - p.cu_query_lens[q];
     const int32_t kv = p.kv_lens[q];
@@ -157,6 +198,8 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
     if (chunk >= longest) chunk = 0;
   }
   s.split_tokens = static_cast<int32_t>(chunk);
+  s.decode.reserve(dec.size() + (chunk > 0 ? static_cast<size_t>(ceil_div(total, chunk)) : 0) +
+                   (p.num_splits > 0 ? dec.size() * static_cast<size_t>(p.num_splits) : 0));
   int64_t slot = 0;
   for (const ua_tile& t : dec) {
     const int64_t len = t.kv_hi - t.kv_lo;
@@ -194,17 +237,17 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
   }
   s.num_slots = slot;
 
-  // 3. Longest work first, so the tail of the grid holds the short tiles.
-  auto longer = [](const ua_tile& a, const ua_tile& b) {
-    const int64_t wa = static_cast<int64_t>(a.kv_hi - a.kv_lo) * a.nrows;
-    const int64_t wb = static_cast<int64_t>(b.kv_hi - b.kv_lo) * b.nrows;
-    if (wa != wb) return wa > wb;
-    if (a.seq != b.seq) return a.seq < b.seq;
-    if (a.kv_head != b.kv_head) return a.kv_head < b.kv_head;
-    if (a.row0 != b.row0) return a.row0 < b.row0;
-    return a.kv_lo < b.kv_lo;
+  // 3. Longest work first, so the tail of the grid holds the short tiles;
+  // equal work in (sequence, KV head, row, key) order, the generation order.
+  auto work_of = [](const ua_tile& t) {
+    return static_cast<int64_t>(t.kv_hi - t.kv_lo) * t.nrows;
   };
-  std::stable_sort(s.decode.begin(), s.decode.end(), longer);
+  {
+    std::vector<SortKey> keys(s.decode.size());
+    for (size_t i = 0; i < s.decode.size(); ++i)
+      keys[i] = {-work_of(s.decode[i]), 0, 0, static_cast<int32_t>(i)};
+    permute(s.decode, order_by(keys));
+  }
   // Prefill tiles stay grouped by (sequence, KV head), longest group first and
   // longest tile first inside a group: CTAs running at the same time then read
   // the same K/V rows, which stay in L2 (a head's K/V is a few MB; all heads
@@ -214,15 +257,14 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
     auto gi = [&](const ua_tile& t) {
       return static_cast<size_t>(t.seq) * p.num_kv_heads + t.kv_head;
     };
-    for (const ua_tile& t : s.prefill)
-      group_work[gi(t)] += static_cast<int64_t>(t.kv_hi - t.kv_lo) * t.nrows;
-    std::stable_sort(s.prefill.begin(), s.prefill.end(),
-                     [&](const ua_tile& a, const ua_tile& b) {
-                       const int64_t ga = group_work[gi(a)], gb = group_work[gi(b)];
-                       if (ga != gb) return ga > gb;
-                       if (gi(a) != gi(b)) return gi(a) < gi(b);
-                       return longer(a, b);
-                     });
+    for (const ua_tile& t : s.prefill) group_work[gi(t)] += work_of(t);
+    std::vector<SortKey> keys(s.prefill.size());
+    for (size_t i = 0; i < s.prefill.size(); ++i) {
+      const ua_tile& t = s.prefill[i];
+      keys[i] = {-group_work[gi(t)], static_cast<int64_t>(gi(t)), -work_of(t),
+                 static_cast<int32_t>(i)};
+    }
+    permute(s.prefill, order_by(keys));
   }
   // Staging pages for an fp8 cache: per sequence with prefill tiles, the
   // logical pages of kStagePage keys from the lowest key any of its tiles
@@ -278,29 +320,26 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
       }
       total_cost += cost[i];
     }
-    std::vector<size_t> by_cost(n);
-    for (size_t i = 0; i < n; ++i) by_cost[i] = i;
-    std::stable_sort(by_cost.begin(), by_cost.end(),
-                     [&](size_t a, size_t b) { return cost[a] < cost[b]; });
+    std::vector<SortKey> keys(n);
+    for (size_t i = 0; i < n; ++i) keys[i] = {cost[i], 0, 0, static_cast<int32_t>(i)};
+    const std::vector<int32_t> by_cost = order_by(keys);
     std::vector<char> in_tail(n, 0);
     int64_t tail_cost = 0;
     for (size_t k = 0; k < n; ++k) {
-      const size_t i = by_cost[k];
+      const size_t i = static_cast<size_t>(by_cost[k]);
       if (static_cast<double>(tail_cost + cost[i]) > kPrefillTailShare * total_cost) break;
       tail_cost += cost[i];
       in_tail[i] = 1;
     }
-    std::vector<ua_tile> bulk, tail;
-    std::vector<int64_t> tail_c;
-    for (size_t i = 0; i < n; ++i) (in_tail[i] ? tail : bulk).push_back(s.prefill[i]);
+    // bulk in list order, then the tail longest first (ties in list order)
+    std::vector<SortKey> tkeys;
+    std::vector<int32_t> order;
+    order.reserve(n);
     for (size_t i = 0; i < n; ++i)
-      if (in_tail[i]) tail_c.push_back(cost[i]);
-    std::vector<size_t> tail_order(tail.size());
-    for (size_t k = 0; k < tail.size(); ++k) tail_order[k] = k;
-    std::stable_sort(tail_order.begin(), tail_order.end(),
-                     [&](size_t a, size_t b) { return tail_c[a] > tail_c[b]; });
-    s.prefill = std::move(bulk);
-    for (size_t k : tail_order) s.prefill.push_back(tail[k]);
+      if (in_tail[i]) tkeys.push_back({-cost[i], 0, 0, static_cast<int32_t>(i)});
+      else order.push_back(static_cast<int32_t>(i));
+    for (int32_t i : order_by(tkeys)) order.push_back(i);
+    permute(s.prefill, order);
     s.prefill_blocks = total_cost;
     s.prefill_ctas = static_cast<int32_t>(std::min<int64_t>(num_sms, static_cast<int64_t>(n)));
   }

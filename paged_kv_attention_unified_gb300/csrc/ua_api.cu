@@ -329,12 +329,25 @@ ua_status ua_schedule(const int32_t* cu_query_lens_host, const int32_t* kv_lens_
   return UA_OK;
 }
 
-ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
-                            const int32_t* kv_lens_host, int32_t num_seqs, int32_t num_q_heads,
-                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                            int32_t max_blocks_per_seq, int32_t kv_dtype, int32_t causal,
-                            int32_t window, int32_t num_splits, int32_t decode_rows_max,
-                            ua_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Plan creation. `extra` (if any): host byte ranges appended, 16-byte
+// aligned, to the plan's one tile-list upload; *extra_dev receives the device
+// address of each (they live as long as the plan).
+struct HostRange {
+  const void* ptr;
+  size_t bytes;
+};
+
+ua_status create_plan(ua_plan** out, const int32_t* cu_query_lens_host,
+                      const int32_t* kv_lens_host, int32_t num_seqs, int32_t num_q_heads,
+                      int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                      int32_t max_blocks_per_seq, int32_t kv_dtype, int32_t causal,
+                      int32_t window, int32_t num_splits, int32_t decode_rows_max,
+                      ua_stream_t stream, const HostRange* extra, int n_extra,
+                      void** extra_dev) {
   if (out == nullptr) return UA_ERR_INVALID_ARG;
   *out = nullptr;
   int dev = 0, sms = 0;
@@ -373,7 +386,13 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   const size_t n_stage = s.stage.size(), n_st = s.staged_table.size();
   const size_t off_stage = off_app + n_app * sizeof(ua_tile);
   const size_t off_st = off_stage + n_stage * sizeof(ua_tile);
-  const size_t bytes_meta = off_st + n_st * sizeof(int32_t);
+  size_t bytes_meta = off_st + n_st * sizeof(int32_t);
+  std::vector<size_t> off_extra(static_cast<size_t>(n_extra > 0 ? n_extra : 0));
+  for (int i = 0; i < n_extra; ++i) {
+    bytes_meta = (bytes_meta + 15) & ~static_cast<size_t>(15);
+    off_extra[i] = bytes_meta;
+    bytes_meta += extra[i].bytes;
+  }
   PinnedBlock staging;
   if (!pinned_take(bytes_meta, &staging)) {
     delete plan;
@@ -388,6 +407,8 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   if (n_app) std::memcpy(host + off_app, s.append.data(), n_app * sizeof(ua_tile));
   if (n_stage) std::memcpy(host + off_stage, s.stage.data(), n_stage * sizeof(ua_tile));
   if (n_st) std::memcpy(host + off_st, s.staged_table.data(), n_st * sizeof(int32_t));
+  for (int i = 0; i < n_extra; ++i)
+    if (extra[i].bytes) std::memcpy(host + off_extra[i], extra[i].ptr, extra[i].bytes);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   plan->last_stream = cs;
   if (plan_alloc(&plan->d_meta, bytes_meta, plan->device, cs) != cudaSuccess) {
@@ -407,6 +428,7 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   plan->d_append = reinterpret_cast<ua_tile*>(base + off_app);
   plan->d_stage = reinterpret_cast<ua_tile*>(base + off_stage);
   plan->d_staged_table = reinterpret_cast<int32_t*>(base + off_st);
+  for (int i = 0; i < n_extra; ++i) extra_dev[i] = base + off_extra[i];
   if (s.staged_pages > 0) {
     const size_t bytes = static_cast<size_t>(s.staged_pages) * ua::kStagePage *
                          plan->prob.num_kv_heads * head_dim * 2;
@@ -444,6 +466,21 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
   plan->last_stream = cs;
   *out = plan;
   return UA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
+                            const int32_t* kv_lens_host, int32_t num_seqs, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                            int32_t max_blocks_per_seq, int32_t kv_dtype, int32_t causal,
+                            int32_t window, int32_t num_splits, int32_t decode_rows_max,
+                            ua_stream_t stream) {
+  return create_plan(out, cu_query_lens_host, kv_lens_host, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, max_blocks_per_seq, kv_dtype, causal, window,
+                     num_splits, decode_rows_max, stream, nullptr, 0, nullptr);
 }
 
 ua_status ua_plan_create(ua_plan** out, const int32_t* cu_query_lens_host,
@@ -551,7 +588,9 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     pp.window = plan->prob.window;
     pp.score_scale_log2 = kp.score_scale_log2;
     pp.out_scale = kp.v_scale;
-    pp.rows_per_box = pp.block_size < 128 ? pp.block_size : 128;
+    const bool wide = plan->prob.head_dim == 256;
+    pp.rows_per_box = wide ? ua::prefill_wide_rows_per_box(pp.block_size)
+                           : (pp.block_size < 128 ? pp.block_size : 128);
     pp.timeout_ns = plan->wait_timeout_ns;
     pp.debug_flags = plan->debug_flags;
     // Timing: CUDA events around a kernel that runs alone; in a mixed batch
@@ -560,9 +599,11 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     ua_plan::EventPair* ev = nullptr;
     if (mixed) span_begin(mp, 0, &pp.span_start, &pp.span_end);
     else ev = timing_begin(mp, 0, cs);
-    if (ua::launch_prefill(pp, q, pk, pv, plan->total_q, plan->prob.head_dim,
-                           plan->prob.num_kv_heads, cs) != cudaSuccess)
-      return UA_ERR_CUDA;
+    const cudaError_t le =
+        wide ? ua::launch_prefill_wide(pp, q, pk, pv, plan->total_q, plan->prob.num_kv_heads, cs)
+             : ua::launch_prefill(pp, q, pk, pv, plan->total_q, plan->prob.head_dim,
+                                  plan->prob.num_kv_heads, cs);
+    if (le != cudaSuccess) return UA_ERR_CUDA;
     timing_end(ev, cs);
     return UA_OK;
   };
@@ -659,6 +700,78 @@ ua_status ua_forward_oneshot(const void* q, const void* k_cache, const void* v_c
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess &&
       st == UA_OK)
     st = UA_ERR_CUDA;
+  ua_plan_destroy(plan);
+  return st;
+}
+
+ua_status ua_forward_host(const void* q_host, void* out_host, const int32_t* cu_query_lens_host,
+                          const int32_t* kv_lens_host, const int32_t* block_tables_host,
+                          const void* k_cache, const void* v_cache, int32_t num_seqs,
+                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int32_t max_blocks_per_seq, int64_t num_blocks,
+                          int32_t kv_dtype, float scale, int32_t causal, int32_t window,
+                          float k_scale, float v_scale, int32_t num_splits,
+                          int32_t* error_word, ua_stream_t stream) {
+  if (num_seqs < 0 || max_blocks_per_seq < 0 || num_q_heads <= 0 || head_dim <= 0)
+    return UA_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (!cu_query_lens_host || !kv_lens_host || !block_tables_host))
+    return UA_ERR_INVALID_ARG;
+  // The query count sizes the q / output buffers, which go first so that
+  // the copy of q runs while the host schedules the batch.
+  int64_t total_q = 0;
+  if (num_seqs > 0) {
+    if (cu_query_lens_host[0] != 0) return UA_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < num_seqs; ++i)
+      if (cu_query_lens_host[i + 1] < cu_query_lens_host[i]) return UA_ERR_INVALID_ARG;
+    total_q = cu_query_lens_host[num_seqs];
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const size_t q_bytes =
+      static_cast<size_t>(total_q) * static_cast<size_t>(num_q_heads) * head_dim * 2;
+  void* dq = nullptr;
+  int dev = 0;
+  if (q_bytes > 0) {
+    if (!q_host || !out_host) return UA_ERR_INVALID_ARG;
+    if (cudaGetDevice(&dev) != cudaSuccess) return UA_ERR_CUDA;
+    if (plan_alloc(&dq, 2 * q_bytes, dev, cs) != cudaSuccess) return UA_ERR_CUDA;
+    if (cudaMemcpyAsync(dq, q_host, q_bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess) {
+      cudaFreeAsync(dq, cs);
+      return UA_ERR_CUDA;
+    }
+  }
+  const HostRange extra[3] = {
+      {cu_query_lens_host, (static_cast<size_t>(num_seqs) + 1) * sizeof(int32_t)},
+      {kv_lens_host, static_cast<size_t>(num_seqs) * sizeof(int32_t)},
+      {block_tables_host,
+       static_cast<size_t>(num_seqs) * static_cast<size_t>(max_blocks_per_seq) * sizeof(int32_t)}};
+  void* dev_extra[3] = {nullptr, nullptr, nullptr};
+  ua_plan* plan = nullptr;
+  ua_status st = create_plan(&plan, cu_query_lens_host, kv_lens_host, num_seqs, num_q_heads,
+                             num_kv_heads, head_dim, block_size, max_blocks_per_seq, kv_dtype,
+                             causal, window, num_splits, -1, stream,
+                             num_seqs > 0 ? extra : nullptr, num_seqs > 0 ? 3 : 0, dev_extra);
+  if (st != UA_OK) {
+    if (dq) cudaFreeAsync(dq, cs);
+    return st;
+  }
+  if (q_bytes > 0) {
+    void* dout = static_cast<uint8_t*>(dq) + q_bytes;
+    st = ua_forward(plan, dq, k_cache, v_cache, dout, static_cast<const int32_t*>(dev_extra[0]),
+                    static_cast<const int32_t*>(dev_extra[1]),
+                    static_cast<const int32_t*>(dev_extra[2]), num_blocks, plan->sched.max_q,
+                    plan->sched.max_kv, scale, k_scale, v_scale, stream);
+    if (st == UA_OK &&
+        cudaMemcpyAsync(out_host, dout, q_bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+      st = UA_ERR_CUDA;
+    if (st == UA_OK && error_word != nullptr &&
+        cudaMemcpyAsync(error_word, plan->d_err, sizeof(int32_t), cudaMemcpyDeviceToHost, cs) !=
+            cudaSuccess)
+      st = UA_ERR_CUDA;
+    cudaFreeAsync(dq, cs);
+  } else if (error_word != nullptr) {
+    *error_word = UA_OK;
+  }
+  if (cudaStreamSynchronize(cs) != cudaSuccess && st == UA_OK) st = UA_ERR_CUDA;
   ua_plan_destroy(plan);
   return st;
 }

@@ -160,7 +160,15 @@ def _check_schedule(cu, kv, hq, hkv, causal=1, window=0, num_splits=0, num_sms=1
     # longest-first order
     work = [(t["kv_hi"] - t["kv_lo"]) * t["nrows"] for t in dec]
     assert work == sorted(work, reverse=True)
-    assert info.num_prefill_ctas == min(num_sms, len(pre))
+    # equal work keeps (sequence, KV head, row, key) order
+    key = lambda t: (t["seq"], t["kv_head"], t["row0"], t["kv_lo"])
+    for a, b, wa, wb in zip(dec, dec[1:], work, work[1:]):
+        if wa == wb:
+            assert key(a) < key(b)
+    if not dec:
+        assert info.num_prefill_ctas == min(num_sms, len(pre))
+    else:
+        assert 1 <= info.num_prefill_ctas <= min(num_sms, len(pre)) or not pre
     return info, pre, dec, grp
 
 
@@ -354,10 +362,16 @@ def test_append_rejects_a_null_plan_without_touching_cuda():
     assert st == ua.UA_ERR_INVALID_ARG
 
 
-def test_head_dim_256_is_decode_only():
-    """head_dim 256 runs in the decode kernel (the prefill kernel takes 64 and
-    128): every row, long prefills included, lands in decode tiles."""
+def test_head_dim_256_prefills_go_to_the_wide_prefill_kernel():
+    """head_dim 256: long prefills run in the wide (one 128-row query tile,
+    64-key tiles) prefill kernel, single tokens in the decode kernel; block
+    sizes that do not divide or are not divided by 64 keep everything in the
+    decode kernel. Every row lands in exactly one tile."""
     info, pre, dec, grp = ua.ua_schedule([0, 1, 301], [500, 800], 8, 2, 256, 16, 64)
+    assert info.num_prefill_tiles > 0 and info.num_decode_tiles > 0
+    assert {t["seq"] for t in pre} == {1} and {t["seq"] for t in dec} == {0}
+    rows = {(t["seq"], t["kv_head"], r) for t in pre + dec
+            for r in range(t["row0"], t["row0"] + t["nrows"])}
+    assert len(rows) == (1 + 300) * 4 * 2
+    info, pre, dec, _ = ua.ua_schedule([0, 1, 301], [500, 800], 8, 2, 256, 48, 17)
     assert info.num_prefill_tiles == 0 and info.num_decode_tiles > 0
-    rows = {(t["seq"], t["kv_head"], r) for t in dec for r in range(t["row0"], t["row0"] + t["nrows"])}
-    assert len(rows) == 301 * 4 * 2

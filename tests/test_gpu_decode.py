@@ -181,6 +181,31 @@ def test_oneshot_matches_plan_path():
     assert torch.equal(a.view(torch.int16), out.cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+def test_host_buffer_entry_point_matches_plan_path(pinned):
+    """ua_forward_host (q, output, lengths and page tables in host memory)
+    gives the planned path's output bit for bit, on a mixed batch (both
+    kernels) and on a decode batch, from pinned and from pageable memory."""
+    for case in (W.make_case("host_mixed", [1, 300, 1, 40], [900, 700, 3000, 40], 16, 4, 128, 16,
+                             seed=81),
+                 W.random_small_case(82, kv_dtype=W.FP8, head_dim=64, num_q_heads=8,
+                                     num_kv_heads=2, max_kv=700)):
+        b = tu.to_device(case)
+        ref = tu.run(case)
+        q_h = case.q.contiguous()
+        out_h = torch.empty_like(q_h)
+        cu_h, kv_h = case.cu_query_lens.to(torch.int32), case.kv_lens.to(torch.int32)
+        bt_h = case.block_tables.to(torch.int32).contiguous()
+        if pinned:
+            q_h, out_h, cu_h, kv_h, bt_h = (t.pin_memory() for t in (q_h, out_h, cu_h, kv_h, bt_h))
+        err = ua.ua_forward_host(q_h, out_h, cu_h, kv_h, bt_h, b.k_cache, b.v_cache,
+                                 b.num_q_heads, b.num_kv_heads, b.head_dim, b.block_size,
+                                 b.num_blocks, b.kv_dtype, b.scale, causal=b.causal,
+                                 window=b.window, k_scale=b.k_scale, v_scale=b.v_scale)
+        assert err == 0
+        assert torch.equal(out_h.view(torch.int16), ref.view(torch.int16)), case.name
+
+
 @pytest.mark.parametrize("cfg", [2, 5, 7, 8])
 def test_full_size_decode_configs_whole_output(cfg):
     """The full-size decode workloads in the benchmark's launch configuration

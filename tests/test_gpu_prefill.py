@@ -236,3 +236,106 @@ def test_many_ragged_sequences_through_both_kernels():
         assert plan.last_device_error() == 0
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     assert_close(as_f64(out), oracle_full_parallel(case), case.kv_dtype, case.name, report=True)
+
+
+# ---- head_dim 256: the wide prefill kernel (one 128-row query tile, 64-key tiles)
+
+def _check_wide(case, decode_rows_max=0):
+    b = tu.to_device(case)
+    with tu.make_plan(b, decode_rows_max=decode_rows_max) as plan:
+        assert plan.info.num_prefill_tiles > 0
+        out = tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    return assert_close(as_f64(out), oracle_full(case), case.kv_dtype, case.name)
+
+
+@pytest.mark.parametrize("qpk,hkv,bs", [(1, 2, 16), (2, 2, 32), (4, 1, 64), (8, 1, 128),
+                                        (4, 2, 16)])
+def test_wide_prefill_matches_oracle(qpk, hkv, bs):
+    """Ragged prefills with contexts that are not multiples of 16 or 64, and a
+    query tile that straddles the 128-row item boundary."""
+    _check_wide(W.make_case(f"wide_{qpk}_{bs}", [300, 77, 129, 1], [300, 533, 200, 90],
+                            qpk * hkv, hkv, 256, bs, seed=700 + bs + qpk))
+
+
+def test_wide_prefill_window_noncausal_poison_and_fp8():
+    _check_wide(W.make_case("wide_win", [400, 260], [900, 260], 8, 2, 256, 16, window=150,
+                            seed=710))
+    _check_wide(W.make_case("wide_nc", [200, 90], [600, 90], 8, 2, 256, 32, causal=False,
+                            seed=711))
+    _check_wide(W.make_case("wide_poison", [333, 150], [700, 181], 8, 2, 256, 16, poison=True,
+                            seed=712))
+    _check_wide(W.make_case("wide_fp8", [300, 77, 150], [300, 500, 460], 8, 2, 256, 16,
+                            kv_dtype=W.FP8, seed=713))
+
+
+def test_wide_prefill_mixed_with_decode_and_repeated():
+    """Long prefills in the wide prefill kernel and single tokens in the
+    head_dim 256 decode kernel, one plan, both grids overlapping; a second
+    forward on the same plan gives the same bits."""
+    case = W.make_case("wide_mixed", [1, 600, 1, 1, 37, 900], [3000, 1400, 70, 5000, 37, 900],
+                       16, 4, 256, 16, seed=720)
+    b = tu.to_device(case)
+    with tu.make_plan(b) as plan:
+        assert plan.info.num_prefill_tiles > 0 and plan.info.num_decode_tiles > 0
+        out = tu.forward(plan, b)
+        out2 = tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert_close(as_f64(out), oracle_full(case), case.kv_dtype, case.name)
+
+
+def test_wide_prefill_bounded_wait_reports_timeout_and_context_survives():
+    case = W.make_case("wide_timeout", [256], [256], 4, 4, 256, 16, seed=730)
+    b = tu.to_device(case)
+    with tu.make_plan(b, decode_rows_max=0) as plan:
+        ua.ua_plan_set_debug(plan.handle, 1, 50_000_000)
+        tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == ua.UA_ERR_DEVICE_TIMEOUT
+        ua.ua_plan_set_debug(plan.handle, 0, 0)
+        out = tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    assert_close(as_f64(out), oracle_full(case), W.BF16, "wide, after timeout")
+
+
+def test_full_size_wide_dense_prefill_whole_output_and_first_row_exact():
+    """Config 4's shape at head_dim 256 through the wide prefill kernel: every
+    element against the fp64 oracle, row 0 of every (sequence, head) equal to
+    V[0] bit for bit."""
+    case = W.config9_dense_prefill_d256()
+    b = tu.to_device(case)
+    with tu.make_plan(b) as plan:
+        assert plan.info.num_decode_tiles == 0 and plan.info.num_prefill_tiles > 0
+        out = tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    got = out.cpu()
+    for s in range(case.num_seqs):
+        page = int(case.block_tables[s, 0])
+        for h in range(case.num_q_heads):
+            assert torch.equal(got[4096 * s, h].view(torch.int16),
+                               case.v_cache[page, 0, h].view(torch.int16))
+    del b, out
+    torch.cuda.empty_cache()
+    assert_close(as_f64(got), oracle_full_parallel(case), case.kv_dtype,
+                 f"workload 9 ({case.name})", report=True)
+
+
+@pytest.mark.parametrize("d", [128, 256])
+def test_one_persistent_cta_runs_every_tile_in_turn(d):
+    """One prefill CTA takes every work tile of the batch in sequence, so every
+    barrier phase, ring position and TMEM buffer runs on across many tiles
+    (a waiter that is a phase away from its barrier shows up here)."""
+    case = W.make_case(f"one_cta_{d}", [1024] * 4, [1024] * 4, 8, 8, d, 128, table="identity",
+                       seed=740 + d)
+    b = tu.to_device(case)
+    with tu.make_plan(b) as plan:
+        ua.ua_plan_set_prefill_ctas(plan.handle, 1)
+        out = tu.forward(plan, b)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    assert_close(as_f64(out), oracle_full(case), case.kv_dtype, case.name)

@@ -289,6 +289,15 @@ def config8_pure_decode_d256(seed: int = 0, poison: bool = False) -> Case:
                      gen=gen, poison=poison)
 
 
+def config9_dense_prefill_d256(seed: int = 0, poison: bool = False) -> Case:
+    """Config 4's dense causal prefill at head_dim 256: batch 4, 32 heads
+    (MHA), q = kv = 4096, bf16, block_size 128, identity table (not one of the
+    five benchmark configurations: it measures the head_dim 256 prefill
+    kernel)."""
+    return make_case("dense_causal_prefill_b4_h32_l4096_d256", [4096] * 4, [4096] * 4, 32, 32,
+                     256, 128, table="identity", seed=seed, poison=poison)
+
+
 CONFIGS = {
     1: config1_tiny_mixed,
     2: config2_pure_decode,
@@ -298,6 +307,7 @@ CONFIGS = {
     6: config6_dense_prefill_fp8,
     7: config7_uniform_decode,
     8: config8_pure_decode_d256,
+    9: config9_dense_prefill_d256,
 }
 
 
