@@ -307,7 +307,7 @@ def _traffic_record(kernel: str, cfg: int):
     the current sources (profiles/traffic.json: {key: {"source_hash", "bytes"}}).
     Returns (bytes or None, note, {"current": digest, "record": digest})."""
     from paged_kv_attention_unified_gb300 import build as B
-    cur = B._digest()
+    cur = B.kernel_digest(kernel)
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(f"{kernel}/workload{cfg}")
@@ -454,7 +454,8 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
         r["timing"] = ("device global-timer span, first CTA start to last CTA end (the two "
                        "kernels of a mixed step overlap), over K steps after the timed ones") \
             if mixed else "CUDA events on the launching stream, over K steps after the timed ones"
-        traffic, note, digests = _traffic_record(kind, cfg)
+        traffic, note, digests = _traffic_record(
+            "prefill_wide" if kind == "prefill" and case.head_dim == 256 else kind, cfg)
         r["traffic"] = traffic
         if note:
             r["traffic_note"] = note

@@ -44,15 +44,33 @@ def sources():
 _SOURCE_SUFFIXES = (".cu", ".cuh", ".cpp", ".h")
 
 
-def _digest(extra=()):
+# What a kernel's DRAM traffic depends on: its own source, the shared device
+# headers, the scheduler (the tiles it launches) and the TMA map encoding.
+_KERNEL_SOURCES = {
+    "decode": ("decode.cu",),
+    "prefill": ("prefill.cu",),
+    "prefill_wide": ("prefill_wide.cu",),
+    "append": ("append.cu",),
+    "stage": ("stage.cu",),
+}
+_SHARED_SOURCES = ("sm100.cuh", "ua_device.cuh", "ua_kernels.h", "tma_host.cu", "planner.cpp",
+                   "planner.h", "ua.h")
+
+
+def kernel_digest(kernel: str) -> str:
+    """Digest of the sources one kernel's DRAM traffic depends on (committed
+    ncu traffic records are keyed by it)."""
+    return _digest(only=_KERNEL_SOURCES[kernel] + _SHARED_SOURCES)
+
+
+def _digest(extra=(), only=None):
     """Hash of the library's sources (by file name, not path) and its compile
     flags with the include paths taken out: the same tree gives the same
-    digest wherever it is checked out (committed ncu traffic records are keyed
-    by it)."""
+    digest wherever it is checked out. only: restrict to these file names."""
     h = hashlib.sha256()
     files = [(f, CSRC) for f in os.listdir(CSRC)] + [(f, INCLUDE) for f in os.listdir(INCLUDE)]
     for name, base in sorted(files):
-        if not name.endswith(_SOURCE_SUFFIXES):
+        if not name.endswith(_SOURCE_SUFFIXES) or (only is not None and name not in only):
             continue
         with open(os.path.join(base, name), "rb") as fh:
             h.update(name.encode())
