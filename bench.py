@@ -486,6 +486,7 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
         h2d = q_h.numel() * 2 + cu_h.numel() * 4 + kv_h.numel() * 4 + bt_h.numel() * 4 + tiles_b
         d2h = out_h.numel() * 2 + 4
         torch.cuda.synchronize()
+        handle = torch.cuda.current_stream().cuda_stream   # the stream every step runs on
         tot = 0.0
         for it in range(args.warmup + args.steps):
             if flush is not None:
@@ -496,7 +497,7 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
                                      b.num_q_heads, b.num_kv_heads, b.head_dim, b.block_size,
                                      b.num_blocks, b.kv_dtype, b.scale, causal=b.causal,
                                      window=b.window, k_scale=b.k_scale, v_scale=b.v_scale,
-                                     num_splits=args.num_splits)
+                                     num_splits=args.num_splits, stream=handle)
             if it >= args.warmup:
                 tot += time.perf_counter() - t_0
             assert err == 0, f"device error word {err}"

@@ -243,10 +243,24 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
     return static_cast<int64_t>(t.kv_hi - t.kv_lo) * t.nrows;
   };
   {
-    std::vector<SortKey> keys(s.decode.size());
-    for (size_t i = 0; i < s.decode.size(); ++i)
-      keys[i] = {-work_of(s.decode[i]), 0, 0, static_cast<int32_t>(i)};
-    permute(s.decode, order_by(keys));
+    const size_t nd = s.decode.size();
+    int64_t max_work = 0;
+    for (const ua_tile& t : s.decode) max_work = std::max(max_work, work_of(t));
+    if (nd < (size_t{1} << 24) && max_work < (int64_t{1} << 39)) {
+      // one 64-bit key per tile: (max_work - work) above a 24-bit index
+      std::vector<uint64_t> keys(nd);
+      for (size_t i = 0; i < nd; ++i)
+        keys[i] = (static_cast<uint64_t>(max_work - work_of(s.decode[i])) << 24) | i;
+      std::sort(keys.begin(), keys.end());
+      std::vector<int32_t> order(nd);
+      for (size_t i = 0; i < nd; ++i) order[i] = static_cast<int32_t>(keys[i] & 0xFFFFFFu);
+      permute(s.decode, order);
+    } else {
+      std::vector<SortKey> keys(nd);
+      for (size_t i = 0; i < nd; ++i)
+        keys[i] = {-work_of(s.decode[i]), 0, 0, static_cast<int32_t>(i)};
+      permute(s.decode, order_by(keys));
+    }
   }
   // Prefill tiles stay grouped by (sequence, KV head), longest group first and
   // longest tile first inside a group: CTAs running at the same time then read

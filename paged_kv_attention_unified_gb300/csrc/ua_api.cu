@@ -20,7 +20,7 @@ struct ua_plan {
   ua::Schedule sched;
   ua_plan_info info{};
   // device memory owned by the plan
-  void* d_meta = nullptr;          // [prefill tiles | decode tiles | groups | error word]
+  void* d_meta = nullptr;          // [tiles | groups | error word | counters | ... | split workspace]
   ua_tile* d_prefill = nullptr;
   ua_tile* d_decode = nullptr;
   ua_combine_group* d_groups = nullptr;
@@ -32,7 +32,7 @@ struct ua_plan {
   ua_tile* d_stage = nullptr;             // fp8 prefill: stage tiles
   void* d_staged_k = nullptr;             // fp8 prefill: bf16 staging caches
   void* d_staged_v = nullptr;
-  float* d_ws = nullptr;           // split workspace: partial rows then lse values
+  // split workspace (inside d_meta): partial rows then lse values
   float* d_ws_o = nullptr;
   float* d_ws_lse = nullptr;
   cudaStream_t last_stream = nullptr;
@@ -154,11 +154,9 @@ void free_plan_memory(ua_plan* p) {
   if (p->d_span) cudaFreeAsync(p->d_span, p->last_stream);
   p->d_span = nullptr;
   if (p->d_meta) cudaFreeAsync(p->d_meta, p->last_stream);
-  if (p->d_ws) cudaFreeAsync(p->d_ws, p->last_stream);
   if (p->d_staged_k) cudaFreeAsync(p->d_staged_k, p->last_stream);
   if (p->d_staged_v) cudaFreeAsync(p->d_staged_v, p->last_stream);
   p->d_meta = nullptr;
-  p->d_ws = nullptr;
   p->d_staged_k = nullptr;
   p->d_staged_v = nullptr;
 }
@@ -411,7 +409,11 @@ ua_status create_plan(ua_plan** out, const int32_t* cu_query_lens_host,
     if (extra[i].bytes) std::memcpy(host + off_extra[i], extra[i].ptr, extra[i].bytes);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   plan->last_stream = cs;
-  if (plan_alloc(&plan->d_meta, bytes_meta, plan->device, cs) != cudaSuccess) {
+  // The split workspace follows the uploaded part in the same allocation
+  // (not copied: every slot is written before it is read).
+  const size_t off_ws = (bytes_meta + 255) & ~static_cast<size_t>(255);
+  const size_t bytes_alloc = off_ws + static_cast<size_t>(plan->info.workspace_bytes);
+  if (plan_alloc(&plan->d_meta, bytes_alloc, plan->device, cs) != cudaSuccess) {
     plan->d_meta = nullptr;
     pinned_give_back(staging);
     free_plan_memory(plan);
@@ -441,16 +443,7 @@ ua_status create_plan(ua_plan** out, const int32_t* cu_query_lens_host,
     }
   }
   if (plan->info.workspace_bytes > 0) {
-    if (plan_alloc(reinterpret_cast<void**>(&plan->d_ws),
-                   static_cast<size_t>(plan->info.workspace_bytes), plan->device,
-                   cs) != cudaSuccess) {
-      plan->d_ws = nullptr;
-      pinned_give_back(staging);
-      free_plan_memory(plan);
-      delete plan;
-      return UA_ERR_CUDA;
-    }
-    plan->d_ws_o = static_cast<float*>(plan->d_ws);
+    plan->d_ws_o = reinterpret_cast<float*>(base + off_ws);
     plan->d_ws_lse = plan->d_ws_o + s.num_slots * UA_DECODE_ROWS * static_cast<int64_t>(head_dim);
   }
   const bool copied =
