@@ -41,12 +41,13 @@
  * the "Fused Attention" notes). It replaces the per-program binary search over
  * the query prefix sums that the vLLM kernel performs at run time.
  *
- * Supported: head_dim 64, 128 and 256, each with a prefill and a decode
- * kernel (the head_dim 256 prefill kernel works on one 128-row query tile and
- * 64-key tiles at a time and takes block sizes that 64 divides or that
- * divide 64); block_size a multiple of 16; any GQA ratio (the prefill
- * kernels take ratios dividing 128; sequences they cannot take run in the
- * decode kernel).
+ * Supported: every head_dim that is a multiple of 32 from 32 to 256 in the
+ * decode kernel, which also runs any prefill no prefill kernel takes; a
+ * tcgen05 prefill kernel at head_dim 64 and 128 (256-row tiles, 128-key
+ * tiles) and one at head_dim 192 and 256 (one 128-row query tile and 64-key
+ * tiles at a time, block sizes that 64 divides or that divide 64);
+ * block_size a multiple of 16; any GQA ratio (the prefill kernels take ratios
+ * dividing 128; sequences they cannot take run in the decode kernel).
  *
  * Conventions.
  *  - The caller owns every tensor argument; the plan owns its device tile list,
@@ -55,8 +56,10 @@
  *    stream-ordered from a pool the library keeps per device), and frees them
  *    in ua_plan_destroy.
  *  - Device pointers must be 16-byte aligned and tensors contiguous.
- *  - All device work is ordered on the stream argument (a mixed batch's
- *    decode half runs on a side stream forked from and joined back into it);
+ *  - All device work is ordered on the stream argument (in a mixed batch the
+ *    decode grid is launched behind the prefill grid on that stream with
+ *    programmatic stream serialization, so that it starts on the SMs the
+ *    prefill grid leaves free);
  *    nothing synchronises the host except ua_last_device_error,
  *    ua_plan_kernel_times, ua_forward_oneshot and ua_forward_host.
  *  - No entry point calls exit, abort or a device trap. Invalid arguments are
@@ -144,9 +147,10 @@ typedef struct ua_plan ua_plan;
  * UA_MAX_SPLITS. num_sms <= 0 means 152.
  * decode_rows_max: sequences with q_len * qpk <= this value go to the decode
  * kernel, the others to a prefill kernel (when one takes the problem:
- * 128 % qpk == 0, and a bf16 cache whose block_size and the key tile (128
- * keys at head dim 64 / 128, 64 at head dim 256) divide one another, or any
- * fp8 cache); < 0 means the built-in default (32).
+ * head_dim 64, 128, 192 or 256, 128 % qpk == 0, and a bf16 cache whose
+ * block_size and the key tile (128 keys at head dim 64 / 128, 64 at head dim
+ * 192 / 256) divide one another, or any fp8 cache); < 0 means the built-in
+ * default (32).
  * The prefill list is in the order the persistent prefill CTAs take it
  * (grouped by sequence and KV head, the shortest tiles last); the decode list
  * is longest first.
@@ -211,10 +215,10 @@ ua_status ua_plan_create_ex(ua_plan** out, const int32_t* cu_query_lens_host,
  * scale: multiplies q.k as given (not assumed to be 1/sqrt(d)).
  * Launches the prefill kernel (after the staging kernel for an fp8 cache)
  * and the decode kernel (which merges split pieces itself) in the order of
- * `stream`: when the batch has both, the decode kernel runs on a side stream
- * of the library's pool that starts once every prefill CTA has begun (so
- * after everything queued on `stream` before the call) and that `stream`
- * waits for: the prefill CTAs hold num_prefill_ctas SMs and the decode CTAs
+ * `stream`: when the batch has both, the decode grid follows the prefill grid
+ * on `stream` as a programmatic dependent launch that may start once every
+ * prefill CTA has begun (so after everything queued on `stream` before the
+ * call): the prefill CTAs hold num_prefill_ctas SMs and the decode CTAs
  * stream the cache on the others, then on the prefill SMs as they free up.
  * Work queued on `stream` afterwards sees the whole result. Not thread-safe per plan:
  * calls that share a plan must be ordered (they share its split workspace).

@@ -10,7 +10,7 @@
 //
 // One CTA per combine group (one decode tile cut into pieces): warp n owns
 // packed row n, every lane a contiguous run of head_dim/32 dimensions, so the
-// partial rows are read with 16-byte (or 8-byte) coalesced loads.
+// partial rows are read with coalesced 16-, 8- or 4-byte loads.
 #include "ua_device.cuh"
 #include "ua_kernels.h"
 
@@ -61,10 +61,16 @@ __global__ void __launch_bounds__(32 * UA_DECODE_ROWS) combine_kernel(const Comb
         acc[e + 2] += w * v.z;
         acc[e + 3] += w * v.w;
       }
+    } else if constexpr (kPer % 2 == 0) {
+#pragma unroll
+      for (int e = 0; e < kPer; e += 2) {
+        const float2 v = *reinterpret_cast<const float2*>(src + e);
+        acc[e] += w * v.x;
+        acc[e + 1] += w * v.y;
+      }
     } else {
-      const float2 v = *reinterpret_cast<const float2*>(src);
-      acc[0] += w * v.x;
-      acc[1] += w * v.y;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) acc[e] += w * src[e];
     }
   }
   const int r = grp.row0 + n;
@@ -78,8 +84,14 @@ __global__ void __launch_bounds__(32 * UA_DECODE_ROWS) combine_kernel(const Comb
       *reinterpret_cast<uint2*>(dst + 2 * e) =
           make_uint2(pack2<false>(acc[e] * inv, acc[e + 1] * inv),
                      pack2<false>(acc[e + 2] * inv, acc[e + 3] * inv));
+  } else if constexpr (kPer % 2 == 0) {
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2)
+      *reinterpret_cast<uint32_t*>(dst + 2 * e) = pack2<false>(acc[e] * inv, acc[e + 1] * inv);
   } else {
-    *reinterpret_cast<uint32_t*>(dst) = pack2<false>(acc[0] * inv, acc[1] * inv);
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      *reinterpret_cast<__nv_bfloat16*>(dst + 2 * e) = __float2bfloat16_rn(acc[e] * inv);
   }
 }
 
@@ -113,12 +125,18 @@ __global__ void gather_debug_kernel(const KernelParams p, const int64_t* row_off
 
 cudaError_t launch_combine(const CombineParams& c, int head_dim, cudaStream_t stream) {
   if (c.num_groups <= 0) return cudaSuccess;
-  if (head_dim == 256)
-    combine_kernel<256><<<c.num_groups, 32 * UA_DECODE_ROWS, 0, stream>>>(c);
-  else if (head_dim == 128)
-    combine_kernel<128><<<c.num_groups, 32 * UA_DECODE_ROWS, 0, stream>>>(c);
-  else
-    combine_kernel<64><<<c.num_groups, 32 * UA_DECODE_ROWS, 0, stream>>>(c);
+  const dim3 grid(static_cast<unsigned>(c.num_groups)), block(32 * UA_DECODE_ROWS);
+  switch (head_dim) {
+    case 32: combine_kernel<32><<<grid, block, 0, stream>>>(c); break;
+    case 64: combine_kernel<64><<<grid, block, 0, stream>>>(c); break;
+    case 96: combine_kernel<96><<<grid, block, 0, stream>>>(c); break;
+    case 128: combine_kernel<128><<<grid, block, 0, stream>>>(c); break;
+    case 160: combine_kernel<160><<<grid, block, 0, stream>>>(c); break;
+    case 192: combine_kernel<192><<<grid, block, 0, stream>>>(c); break;
+    case 224: combine_kernel<224><<<grid, block, 0, stream>>>(c); break;
+    case 256: combine_kernel<256><<<grid, block, 0, stream>>>(c); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

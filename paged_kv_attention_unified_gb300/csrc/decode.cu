@@ -33,29 +33,61 @@
 // same launch (otherwise the combine kernel does).
 #include "sm100.cuh"
 #include "ua_device.cuh"
+#include "planner.h"
 #include "ua_kernels.h"
 
 namespace ua {
 
 namespace {
 
+// Values per shared-memory load: as many as fill 16 bytes, else 8 or 4 bytes,
+// dividing the n values a lane reads per row.
+constexpr int load_vals(int n, int elt) {
+  int v = 16 / elt;
+  while (v * elt > 4 && n % v != 0) v /= 2;
+  return v;
+}
+
+// Head dims: any multiple of 32 up to 256.
 template <int D, bool FP8>
 struct DecodeCfg {
+  static_assert(D % 32 == 0 && D >= 32 && D <= 256, "head_dim");
   static constexpr int ELT = FP8 ? 1 : 2;                       // cache element bytes
-  static constexpr int KE = (16 / ELT) < (D / 4) ? (16 / ELT) : (D / 4);  // K values per load
   static constexpr int KVALS = D / 4;                           // K values per row per lane
+  static constexpr int KE = load_vals(KVALS, ELT);              // K values per load
   static constexpr int KW = KVALS * ELT / 4;                    // ... as 32-bit words
   static constexpr int NKL = KVALS / KE;                        // K loads per row
-  static constexpr int VE = (16 / ELT) < (D / 8) ? (16 / ELT) : (D / 8);  // V values per load
   static constexpr int VVALS = D / 8;                           // V values per key per lane
+  static constexpr int VE = load_vals(VVALS, ELT);              // V values per load
   static constexpr int VW = VVALS * ELT / 4;
   static constexpr int NVL = VVALS / VE;
-  static constexpr int VLB = VE * ELT;                          // bytes per V load (16 or 8)
+  static constexpr int VLB = VE * ELT;                          // bytes per V load (16, 8 or 4)
   static constexpr int NC = D / 16;                             // MMA chunks along D
   static constexpr int QW = KVALS / 2;                          // Q words (16-bit pairs)
+  static_assert(KVALS % KE == 0 && VVALS % VE == 0 && KE * ELT >= 4 && VLB >= 4, "loads");
 };
 
-constexpr int kWarps = 4;
+// A load of B bytes (16, 8 or 4) from shared memory into consecutive words.
+template <int B>
+__device__ __forceinline__ void lds_words(uint32_t* w, const uint8_t* src, bool ok) {
+  if constexpr (B == 16) {
+    uint4 x = make_uint4(0u, 0u, 0u, 0u);
+    if (ok) x = *reinterpret_cast<const uint4*>(src);
+    w[0] = x.x;
+    w[1] = x.y;
+    w[2] = x.z;
+    w[3] = x.w;
+  } else if constexpr (B == 8) {
+    uint2 x = make_uint2(0u, 0u);
+    if (ok) x = *reinterpret_cast<const uint2*>(src);
+    w[0] = x.x;
+    w[1] = x.y;
+  } else {
+    w[0] = ok ? *reinterpret_cast<const uint32_t*>(src) : 0u;
+  }
+}
+
+constexpr int kWarps = kDecodeWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // How far a unified-max reference may sit above a row's first max (log2
@@ -93,11 +125,12 @@ __device__ __forceinline__ int v_dim(int v, int g) {
 // (unswizzled, the 8 K rows at a 256-byte stride share half of the banks).
 // The e4m3 path keeps plain rows: its K reads are half as many and its
 // conversion work leaves no issue slots for the swizzled address arithmetic
-// (measured: slower with the swizzle).
+// (measured: slower with the swizzle). So do bf16 rows that are not a whole
+// number of 128-byte panels (head dims 32, 96, 160, 224).
 template <int D, bool FP8>
 struct PageLayout {
   static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
-  static constexpr bool kSwizzle = !FP8 && kRowBytes >= 128;
+  static constexpr bool kSwizzle = !FP8 && kRowBytes % 128 == 0;
   static constexpr int kBoxDims = kSwizzle ? 128 / (FP8 ? 1 : 2) : D;  // elements per box row
   static constexpr int kPanels = kSwizzle ? kRowBytes / 128 : 1;
   static constexpr int kPanelBytes = 16 * (kSwizzle ? 128 : kRowBytes);
@@ -131,16 +164,11 @@ __device__ __forceinline__ void read_k(StepRegs<D, FP8>& r, const uint8_t* kp, i
   for (int h = 0; h < 2; ++h) {
     const int key = key_of_row(g + 8 * h);
     const bool ok = base + key < kv_hi;
+    constexpr int kB = C::KE * C::ELT;  // bytes per load
 #pragma unroll
-    for (int l = 0; l < C::NKL; ++l) {
-      uint4 x = make_uint4(0u, 0u, 0u, 0u);
-      if (ok)
-        x = *reinterpret_cast<const uint4*>(kp + PL::at(key, (l * 4 * C::KE + t * C::KE) * C::ELT));
-      r.k[h][4 * l + 0] = x.x;
-      r.k[h][4 * l + 1] = x.y;
-      r.k[h][4 * l + 2] = x.z;
-      r.k[h][4 * l + 3] = x.w;
-    }
+    for (int l = 0; l < C::NKL; ++l)
+      lds_words<kB>(&r.k[h][l * (kB / 4)], kp + PL::at(key, (l * 4 * C::KE + t * C::KE) * C::ELT),
+                    ok);
   }
 }
 
@@ -154,22 +182,9 @@ __device__ __forceinline__ void read_v(StepRegs<D, FP8>& r, const uint8_t* vp, i
     const int key = 4 * t + j;
     const bool ok = base + key < kv_hi;
 #pragma unroll
-    for (int l = 0; l < C::NVL; ++l) {
-      const uint8_t* a = vp + PL::at(key, (l * 8 * C::VE + g * C::VE) * C::ELT);
-      if constexpr (C::VLB == 16) {
-        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (ok) x = *reinterpret_cast<const uint4*>(a);
-        r.v[j][4 * l + 0] = x.x;
-        r.v[j][4 * l + 1] = x.y;
-        r.v[j][4 * l + 2] = x.z;
-        r.v[j][4 * l + 3] = x.w;
-      } else {
-        uint2 x = make_uint2(0u, 0u);
-        if (ok) x = *reinterpret_cast<const uint2*>(a);
-        r.v[j][2 * l + 0] = x.x;
-        r.v[j][2 * l + 1] = x.y;
-      }
-    }
+    for (int l = 0; l < C::NVL; ++l)
+      lds_words<C::VLB>(&r.v[j][l * (C::VLB / 4)],
+                        vp + PL::at(key, (l * 8 * C::VE + g * C::VE) * C::ELT), ok);
   }
 }
 
@@ -309,23 +324,26 @@ __device__ __forceinline__ void compute_step(WarpState<D>& st, StepRegs<D, FP8>&
 // Shared memory of one CTA: a ring of R stages per warp, each holding the K
 // and V rows (16 x head_dim, in the page layout above) of one 16-key step as
 // TMA lands them; then one mbarrier per stage. After the loop the ring is
-// reused for the cross-warp merge. About 64 KB, so that three CTAs (twelve
-// warps) share an SM.
+// reused for the cross-warp merge. The sizes come from the scheduler's copy of
+// the decode geometry, which also sizes splits by the CTAs an SM holds.
 template <int D, bool FP8>
 struct Ring {
-  static constexpr int kRowBytes = D * (FP8 ? 1 : 2);
-  static constexpr int kStage = 2 * 16 * kRowBytes;
-  static constexpr int kStages = kStage >= 8192 ? 2 : (kStage >= 4096 ? 4 : 8);
+  static constexpr int kElt = FP8 ? 1 : 2;
+  static constexpr int kRowBytes = D * kElt;
+  static constexpr int kStage = decode_stage_bytes(D, kElt);
+  static constexpr int kStages = decode_ring_stages(D, kElt);
   static constexpr int kRing = kWarps * kStages * kStage;
   static constexpr int kBars = kRing;
   static constexpr int kMisc = kBars + 8 * kWarps * kStages;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment (swizzle atoms)
+  static constexpr int kCtasPerSm = decode_ctas_per_sm(D, kElt);
+  static_assert(kAlloc == decode_smem_bytes(D, kElt), "decode shared memory");
   static_assert(kWarps * UA_DECODE_ROWS * (D + 2) * 4 <= kRing, "merge buffers alias the ring");
 };
 
 template <int D, bool FP8>
-__global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
+__global__ void __launch_bounds__(kThreads, Ring<D, FP8>::kCtasPerSm)
     decode_kernel(const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v, const KernelParams p) {
   using C = DecodeCfg<D, FP8>;
@@ -586,8 +604,13 @@ __global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
       for (int i = 0; i < kSeg / 8; ++i)
         *reinterpret_cast<uint4*>(dst + 16 * i) =
             make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+    } else if constexpr (kSeg % 4 == 0) {
+#pragma unroll
+      for (int i = 0; i < kSeg / 4; ++i)
+        *reinterpret_cast<uint2*>(dst + 8 * i) = make_uint2(packed[2 * i], packed[2 * i + 1]);
     } else {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+#pragma unroll
+      for (int i = 0; i < kSeg / 2; ++i) *reinterpret_cast<uint32_t*>(dst + 4 * i) = packed[i];
     }
   };
   const float inv = L > 0.f ? p.v_scale / L : 0.f;
@@ -599,10 +622,16 @@ __global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
   // Split piece: normalised partial row and its base-2 log-sum-exp.
   if (row_ok) {
     float* wo = p.ws_o + (static_cast<int64_t>(tile.slot) * UA_DECODE_ROWS + n) * D + d0;
+    if constexpr (kSeg % 4 == 0) {
 #pragma unroll
-    for (int e = 0; e < kSeg; e += 4)
-      *reinterpret_cast<float4*>(wo + e) =
-          make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+      for (int e = 0; e < kSeg; e += 4)
+        *reinterpret_cast<float4*>(wo + e) =
+            make_float4(o[e] * inv, o[e + 1] * inv, o[e + 2] * inv, o[e + 3] * inv);
+    } else {
+#pragma unroll
+      for (int e = 0; e < kSeg; e += 2)
+        *reinterpret_cast<float2*>(wo + e) = make_float2(o[e] * inv, o[e + 1] * inv);
+    }
     if (threadIdx.x % 16 == 0)
       p.ws_lse[static_cast<int64_t>(tile.slot) * UA_DECODE_ROWS + n] =
           L > 0.f ? M + log2f(L) : -INFINITY;
@@ -642,13 +671,22 @@ __global__ void __launch_bounds__(kThreads, D > 128 ? 1 : 3)
       W += w;
       const float* src =
           p.ws_o + ((static_cast<int64_t>(grp.slot0) + sp) * UA_DECODE_ROWS + n) * D + d0;
+      if constexpr (kSeg % 4 == 0) {
 #pragma unroll
-      for (int e = 0; e < kSeg; e += 4) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + e));
-        acc[e] += w * v.x;
-        acc[e + 1] += w * v.y;
-        acc[e + 2] += w * v.z;
-        acc[e + 3] += w * v.w;
+        for (int e = 0; e < kSeg; e += 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(src + e));
+          acc[e] += w * v.x;
+          acc[e + 1] += w * v.y;
+          acc[e + 2] += w * v.z;
+          acc[e + 3] += w * v.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < kSeg; e += 2) {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(src + e));
+          acc[e] += w * v.x;
+          acc[e + 1] += w * v.y;
+        }
       }
     }
     store_out(acc, W > 0.f ? 1.f / W : 0.f);
@@ -696,14 +734,18 @@ cudaError_t launch_decode(const KernelParams& p, int head_dim, int kv_dtype, cud
                           bool after_prefill) {
   if (p.num_tiles <= 0) return cudaSuccess;
   const bool a = after_prefill;
-  if (kv_dtype == UA_KV_BF16) {
-    if (head_dim == 256) return launch_decode_d<256, false>(p, stream, a);
-    return head_dim == 128 ? launch_decode_d<128, false>(p, stream, a)
-                           : launch_decode_d<64, false>(p, stream, a);
+  const bool f8 = kv_dtype != UA_KV_BF16;
+  switch (head_dim) {
+    case 32: return f8 ? launch_decode_d<32, true>(p, stream, a) : launch_decode_d<32, false>(p, stream, a);
+    case 64: return f8 ? launch_decode_d<64, true>(p, stream, a) : launch_decode_d<64, false>(p, stream, a);
+    case 96: return f8 ? launch_decode_d<96, true>(p, stream, a) : launch_decode_d<96, false>(p, stream, a);
+    case 128: return f8 ? launch_decode_d<128, true>(p, stream, a) : launch_decode_d<128, false>(p, stream, a);
+    case 160: return f8 ? launch_decode_d<160, true>(p, stream, a) : launch_decode_d<160, false>(p, stream, a);
+    case 192: return f8 ? launch_decode_d<192, true>(p, stream, a) : launch_decode_d<192, false>(p, stream, a);
+    case 224: return f8 ? launch_decode_d<224, true>(p, stream, a) : launch_decode_d<224, false>(p, stream, a);
+    case 256: return f8 ? launch_decode_d<256, true>(p, stream, a) : launch_decode_d<256, false>(p, stream, a);
+    default: return cudaErrorInvalidValue;
   }
-  if (head_dim == 256) return launch_decode_d<256, true>(p, stream, a);
-  return head_dim == 128 ? launch_decode_d<128, true>(p, stream, a)
-                         : launch_decode_d<64, true>(p, stream, a);
 }
 
 }  // namespace ua

@@ -93,7 +93,7 @@ ua_status validate(const Problem& p) {
   if (p.causal != 0 && p.causal != 1) return UA_ERR_INVALID_ARG;
   if (p.num_seqs > 0 && (p.cu_query_lens == nullptr || p.kv_lens == nullptr))
     return UA_ERR_INVALID_ARG;
-  if (p.head_dim != 64 && p.head_dim != 128 && p.head_dim != 256) return UA_ERR_UNSUPPORTED;
+  if (p.head_dim < 32 || p.head_dim > 256 || p.head_dim % 32 != 0) return UA_ERR_UNSUPPORTED;
   if (p.block_size % kKeyStep != 0) return UA_ERR_UNSUPPORTED;
   if (p.num_seqs == 0) return UA_OK;
   if (p.cu_query_lens[0] != 0) return UA_ERR_INVALID_ARG;
@@ -190,7 +190,7 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
   }
   int64_t chunk = 0;  // 0: do not split
   if (p.num_splits == 0 && !dec.empty() && total > 0) {
-    const int64_t slots = static_cast<int64_t>(num_sms) * decode_ctas_per_sm(p.head_dim);
+    const int64_t slots = static_cast<int64_t>(num_sms) * decode_ctas_per_sm(p.head_dim, p.kv_dtype == UA_KV_BF16 ? 2 : 1);
     chunk = round_up(std::max<int64_t>(kMinSplitTokens, ceil_div(total, slots)), kKeyStep);
     chunk = std::max<int64_t>(chunk, round_up(ceil_div(longest, UA_MAX_SPLITS), kKeyStep));
     if (chunk < longest && shortest * 16 >= longest * 15)

@@ -69,11 +69,44 @@ struct Schedule {
 // Granularity of key ranges: one decode step reads 16 tokens, so split pieces
 // and decode ranges start on multiples of 16.
 constexpr int kKeyStep = 16;
-// Decode kernel: resident CTAs per SM (three of 64 KB shared memory each up
-// to head_dim 128, one at head_dim 256), used to size automatic splits:
-// pieces of about the average load of one CTA slot in a single wave, so that
-// long sequences are cut and short ones not.
-constexpr int decode_ctas_per_sm(int head_dim) { return head_dim > 128 ? 1 : 3; }
+// Decode kernel geometry, shared by the kernel and the scheduler. Each of
+// the four warps of a CTA owns a ring of TMA stages, one stage holding the K
+// and V rows of one 16-key step: 16 KB of ring per warp where that gives 2 to
+// 8 stages, two stages at the widest heads.
+constexpr int kDecodeWarps = 4;
+constexpr int decode_stage_bytes(int head_dim, int elt_bytes) {
+  return 2 * kKeyStep * head_dim * elt_bytes;
+}
+constexpr int decode_ring_stages(int head_dim, int elt_bytes) {
+  return 16384 / decode_stage_bytes(head_dim, elt_bytes) < 2
+             ? 2
+             : (16384 / decode_stage_bytes(head_dim, elt_bytes) > 8
+                    ? 8
+                    : 16384 / decode_stage_bytes(head_dim, elt_bytes));
+}
+// Dynamic shared memory of one CTA: the rings, one mbarrier per stage, 16
+// bytes of flags and 1 KB of slack for the 1024-byte alignment of the
+// swizzle atoms.
+constexpr int decode_smem_bytes(int head_dim, int elt_bytes) {
+  return kDecodeWarps * decode_ring_stages(head_dim, elt_bytes) *
+             (decode_stage_bytes(head_dim, elt_bytes) + 8) +
+         16 + 1024;
+}
+// Resident decode CTAs per SM: as many as the 228 KB of shared memory of an
+// SM hold (1 KB of it reserved per CTA), at most three (the register budget
+// of 128-thread CTAs up to head_dim 128) and at most two above head_dim 128.
+// The kernel is compiled for this many CTAs per SM; the scheduler sizes
+// automatic splits with it (pieces of about the average load of one CTA slot
+// in a single wave, so that long sequences are cut and short ones not).
+constexpr int decode_ctas_per_sm(int head_dim, int elt_bytes = 2) {
+  return (233472 / (decode_smem_bytes(head_dim, elt_bytes) + 1024)) < (head_dim > 128 ? 2 : 3)
+             ? 233472 / (decode_smem_bytes(head_dim, elt_bytes) + 1024)
+             : (head_dim > 128 ? 2 : 3);
+}
+static_assert(decode_ctas_per_sm(128) == 3 && decode_ctas_per_sm(256) == 1 &&
+                  decode_ctas_per_sm(256, 1) == 2 && decode_ctas_per_sm(192) == 2 &&
+                  decode_ctas_per_sm(224) == 1 && decode_ctas_per_sm(32) == 3,
+              "decode residency");
 // Cost of one split piece beyond its keys (CTA start, ring fill, merge and
 // store), in key tokens: used when automatic splits are fitted to whole waves.
 constexpr int kPieceOverheadTokens = 128;

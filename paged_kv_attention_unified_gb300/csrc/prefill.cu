@@ -777,7 +777,7 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
 }  // namespace
 
 bool prefill_supported(int head_dim, int kv_dtype, int qpk, int block_size) {
-  if (head_dim == 256) return prefill_wide_supported(kv_dtype, qpk, block_size);
+  if (prefill_is_wide(head_dim)) return prefill_wide_supported(kv_dtype, qpk, block_size);
   return (head_dim == 64 || head_dim == 128) && kv_dtype == UA_KV_BF16 && qpk >= 1 &&
          qpk <= kRows && kRows % qpk == 0 && block_size >= 16 &&
          (kKeys % block_size == 0 || block_size % kKeys == 0);

@@ -1,23 +1,23 @@
-// Prefill kernel for head_dim 256 (K-P, wide heads): tcgen05 / TMEM / TMA
-// attention, persistent, one 128-row query tile at a time.
+// Prefill kernel for head_dim 192 and 256 (K-P, wide heads): tcgen05 / TMEM /
+// TMA attention, persistent, one 128-row query tile at a time.
 //
 // Same work and loop as the head_dim 64 / 128 prefill kernel -- packed rows
 // (tokens x the qpk query heads of one KV head, the packed GQA tile of
 // "vllm_triton_unified_attention_notes") against their causal key prefix, S =
 // Q K^T, online softmax in base 2, O += P V, O / l at the end (the FA2
-// forward of the "Fused Attention" notes) -- laid out for a 256-wide head,
-// whose O alone takes 256 of the 512 TMEM columns and whose Q tile takes 64 KB
-// of shared memory:
+// forward of the "Fused Attention" notes) -- laid out for a wide head D, whose
+// O alone takes D of the 512 TMEM columns and whose Q tile takes D/4 KB of
+// shared memory:
 //   - one query tile of 128 rows per item (the scheduler cuts each 256-row
 //     work tile of the plan into its two query tiles);
 //   - key tiles of 64 keys; S is double-buffered in TMEM (columns 0 and 64),
 //     so the MMA for key tile j+1 runs while the softmax works on tile j,
-//     and O sits in columns 256-511;
-//   - S = Q K^T as tcgen05 SS-MMAs (M 128, N 64, 16 steps of K = 16 along the
-//     head), O += P V as TS-MMAs (M 128, N 256, P read from TMEM where the
+//     and O sits in columns 256 .. 256 + D - 1;
+//   - S = Q K^T as tcgen05 SS-MMAs (M 128, N 64, D / 16 steps of K = 16 along
+//     the head), O += P V as TS-MMAs (M 128, N D, P read from TMEM where the
 //     softmax wrote it over S);
-//   - shared memory: Q 64 KB, a 3-stage K ring and a 2-stage V ring of 32 KB
-//     stages (64 keys x 256 dims, four 128-byte swizzled panels each).
+//   - shared memory: Q (D / 4 KB), a 3-stage K ring and a 2-stage V ring of
+//     D / 8 KB stages (64 keys x D dims, D / 64 128-byte swizzled panels each).
 // Warps: 0 TMA producer of Q and the K ring, 1 TMEM owner and MMA issuer, 2
 // TMA producer of the V ring, 3 scheduler, 4-7 softmax (one row per thread).
 // The rings, barrier phases and S buffers run on across items. Every
@@ -37,20 +37,16 @@ using namespace sm100;
 
 namespace wide {
 
-constexpr int D = 256;
 constexpr int kRows = 128;      // query rows per item (TMEM lanes, MMA M)
 constexpr int kKeys = 64;       // keys per key tile (MMA N of S, K of P V)
 constexpr int kPlanRows = 256;  // rows of one work tile of the plan (two items)
 constexpr int kThreads = 256;   // 8 warps
 constexpr int KS = 3;           // K ring stages
 constexpr int VS = 2;           // V ring stages
-constexpr int kPanels = D / 64;             // 128-byte swizzled panels per row block
 constexpr int kPanelQ = kRows * 128;        // one Q panel: 16 KB
 constexpr int kPanelKV = kKeys * 128;       // one K / V panel: 8 KB
-constexpr int kQBytes = kRows * D * 2;      // 64 KB
-constexpr int kStage = kKeys * D * 2;       // 32 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 256;             // O columns 256..511
+constexpr uint32_t kOCol = 256;             // O columns 256 .. 256 + D - 1
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr int kItemBytes = 64;
 // Arrivals that free the item slot: two producer threads, the MMA thread and
@@ -58,10 +54,16 @@ constexpr int kItemBytes = 64;
 constexpr int kItemConsumers = 3 + 4;
 
 // Shared-memory layout (byte offsets; the ring stages are 1024-byte aligned).
-constexpr int kQ = 0;
-constexpr int kK = kQ + kQBytes;
-constexpr int kV = kK + KS * kStage;
-constexpr int kBar = kV + VS * kStage;
+template <int D>
+struct Geo {
+  static_assert(D == 192 || D == 256, "head_dim of the wide prefill kernel");
+  static constexpr int kPanels = D / 64;           // 128-byte swizzled panels per row block
+  static constexpr int kQBytes = kRows * D * 2;    // 48 / 64 KB
+  static constexpr int kStage = kKeys * D * 2;     // 24 / 32 KB
+  static constexpr int kQ = 0;
+  static constexpr int kK = kQ + kQBytes;
+  static constexpr int kV = kK + KS * kStage;
+  static constexpr int kBar = kV + VS * kStage;
 // q_full, q_empty, kfull[KS], kempty[KS], vfull[VS], vempty[VS], s_full[2],
 // p_ready[2], o_done[2], mma_done, item_full, item_empty. Key tile g uses S
 // buffer g % 2 and the barriers of that parity. A parity wait is only sound
@@ -69,12 +71,13 @@ constexpr int kBar = kV + VS * kStage;
 // double-buffered S the roles run up to two key tiles apart (S(g) is issued
 // before P V(g-1), so the softmax may see S(g) while P V(g-1) still runs):
 // one barrier per buffer keeps every waiter within one phase.
-constexpr int kNumBars = 2 + 2 * KS + 2 * VS + 2 + 2 + 2 + 1 + 2;
-constexpr int kMisc = kBar + 8 * kNumBars;
-constexpr int kItems = kMisc + 64;
-constexpr int kBytes = kItems + kItemBytes;
-constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
-static_assert(kAlloc <= 232448, "shared memory of the wide prefill kernel");
+  static constexpr int kNumBars = 2 + 2 * KS + 2 * VS + 2 + 2 + 2 + 1 + 2;
+  static constexpr int kMisc = kBar + 8 * kNumBars;
+  static constexpr int kItems = kMisc + 64;
+  static constexpr int kBytes = kItems + kItemBytes;
+  static constexpr int kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kAlloc <= 232448, "shared memory of the wide prefill kernel");
+};
 
 struct Bars {
   uint32_t base;
@@ -175,8 +178,10 @@ __device__ __forceinline__ void scheduler_role(const PrefillParams& p, const Bar
 // rows of a larger page) and 64-wide panel. Every page id is read from the
 // block table and checked; a missing or out-of-range page is loaded from an
 // out-of-range block coordinate, which TMA fills with zeros.
+template <int D>
 __device__ __forceinline__ void load_key_tile(const CUtensorMap* map, const PrefillParams& p,
                                               const Item& it, int j, uint8_t* dst, uint32_t full) {
+  constexpr int kPanels = Geo<D>::kPanels, kStage = Geo<D>::kStage;
   const int boxes = kKeys / p.rows_per_box;
   const int base = it.kv_lo + j * kKeys;
   mbar_arrive_expect_tx(full, kStage);
@@ -203,11 +208,12 @@ __device__ __forceinline__ void load_key_tile(const CUtensorMap* map, const Pref
 
 // One thread of warp 0 (Q and the K ring) or of warp 2 (kIsV: the V ring).
 // Ring positions run on across items.
-template <bool kIsV>
+template <int D, bool kIsV>
 __device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CUtensorMap* map_kv,
                                               const PrefillParams& p, const uint8_t* slot,
                                               uint8_t* sQ, uint8_t* sRing, const Bars& bar,
                                               volatile int32_t* abort, volatile int32_t* never) {
+  constexpr int kPanels = Geo<D>::kPanels, kQBytes = Geo<D>::kQBytes, kStage = Geo<D>::kStage;
   constexpr int kStages = kIsV ? VS : KS;
   prefetch_tmap(map_kv);
   if (!kIsV) prefetch_tmap(map_q);
@@ -248,7 +254,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CU
           ok = false;
           break;
         }
-        load_key_tile(map_kv, p, it, j, sRing + s * kStage, kIsV ? bar.vfull(s) : bar.kfull(s));
+        load_key_tile<D>(map_kv, p, it, j, sRing + s * kStage, kIsV ? bar.vfull(s) : bar.kfull(s));
         last_phase[s] = step / kStages;
       }
     }
@@ -268,9 +274,11 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CU
 // ------------------------------------------------------------------ MMA issuer
 // Per item: S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ... | PV(n-1); key tile g
 // (counted across items) uses S buffer g % 2, K and V ring position g.
+template <int D>
 __device__ __forceinline__ void mma_role(const PrefillParams& p, const uint8_t* slot, uint8_t* sQ,
                                          uint8_t* sK, uint8_t* sV, uint32_t tmem, const Bars& bar,
                                          volatile int32_t* abort, volatile int32_t* never) {
+  constexpr int kStage = Geo<D>::kStage;
   constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);
   constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 0, 1);
   // S(g) = Q K(g)^T into S buffer g % 2; the k-th MMA steps 16 head dims,
@@ -351,9 +359,11 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, const uint8_t* 
 // Warps 4-7, one thread per row r (TMEM lane r; warp w may only touch lanes
 // 32 (w % 4) .. + 31). g0: key tiles of earlier items (barrier phases and S
 // buffers).
+template <int D>
 __device__ __forceinline__ bool softmax_item(const PrefillParams& p, const Item& it, int g0,
                                              uint8_t* sV, uint32_t tmem, const Bars& bar,
                                              volatile int32_t* abort, int warp, int lane) {
+  constexpr int kPanels = Geo<D>::kPanels, kStage = Geo<D>::kStage;
   const uint32_t quarter = static_cast<uint32_t>(warp & 3);
   const int r = static_cast<int>(quarter) * 32 + lane;
   const uint32_t lane_addr = (quarter * 32) << 16;
@@ -506,6 +516,7 @@ __device__ __forceinline__ bool softmax_item(const PrefillParams& p, const Item&
   return true;
 }
 
+template <int D>
 __device__ __forceinline__ void softmax_role(const PrefillParams& p, const uint8_t* slot,
                                              uint8_t* sV, uint32_t tmem, const Bars& bar,
                                              volatile int32_t* abort, int warp, int lane) {
@@ -519,7 +530,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const uint8
     __syncwarp();
     if (lane == 0) mbar_arrive(bar.item_empty());
     if (it.end) break;
-    if (!softmax_item(p, it, g0, sV, tmem, bar, abort, warp, lane)) {
+    if (!softmax_item<D>(p, it, g0, sV, tmem, bar, abort, warp, lane)) {
       give_up(p, abort);
       return;
     }
@@ -527,21 +538,23 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const uint8
   }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_wide_kernel(const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_k,
                         const __grid_constant__ CUtensorMap map_v, const PrefillParams p) {
+  using G = Geo<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sQ = sm + kQ;
-  uint8_t* sK = sm + kK;
-  uint8_t* sV = sm + kV;
-  const Bars bar{smem_u32(sm + kBar)};
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc);
-  volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(sm + kMisc + 8);
-  volatile int32_t* never = reinterpret_cast<volatile int32_t*>(sm + kMisc + 12);
-  uint8_t* slot = sm + kItems;
+  uint8_t* sQ = sm + G::kQ;
+  uint8_t* sK = sm + G::kK;
+  uint8_t* sV = sm + G::kV;
+  const Bars bar{smem_u32(sm + G::kBar)};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + G::kMisc);
+  volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(sm + G::kMisc + 8);
+  volatile int32_t* never = reinterpret_cast<volatile int32_t*>(sm + G::kMisc + 12);
+  uint8_t* slot = sm + G::kItems;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // A decode grid queued behind this one with programmatic stream
@@ -581,15 +594,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer_role<false>(&map_q, &map_k, p, slot, sQ, sK, bar, abort, never);
+    if (lane == 0) producer_role<D, false>(&map_q, &map_k, p, slot, sQ, sK, bar, abort, never);
   } else if (warp == 1) {
-    if (lane == 0) mma_role(p, slot, sQ, sK, sV, tmem, bar, abort, never);
+    if (lane == 0) mma_role<D>(p, slot, sQ, sK, sV, tmem, bar, abort, never);
   } else if (warp == 2) {
-    if (lane == 0) producer_role<true>(&map_q, &map_v, p, slot, sQ, sV, bar, abort, never);
+    if (lane == 0) producer_role<D, true>(&map_q, &map_v, p, slot, sQ, sV, bar, abort, never);
   } else if (warp == 3) {
     if (lane == 0) scheduler_role(p, bar, slot, abort);
   } else {
-    softmax_role(p, slot, sV, tmem, bar, abort, warp, lane);
+    softmax_role<D>(p, slot, sV, tmem, bar, abort, warp, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -600,28 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && p.span_end != nullptr) atomicMax(p.span_end, globaltimer_ns());
 }
 
-}  // namespace wide
-}  // namespace
-
-bool prefill_wide_supported(int kv_dtype, int qpk, int block_size) {
-  return kv_dtype == UA_KV_BF16 && qpk >= 1 && qpk <= wide::kRows && wide::kRows % qpk == 0 &&
-         block_size >= 16 && (wide::kKeys % block_size == 0 || block_size % wide::kKeys == 0);
-}
-
-int prefill_wide_rows_per_box(int block_size) {
-  return block_size < wide::kKeys ? block_size : wide::kKeys;
-}
-
-cudaError_t launch_prefill_wide(const PrefillParams& p, const void* q, const void* k_cache,
-                                const void* v_cache, int64_t total_q, int num_kv_heads,
-                                cudaStream_t stream) {
-  using namespace wide;
-  if (p.num_tiles <= 0 || p.num_ctas <= 0) return cudaSuccess;
-  if (p.counters == nullptr || p.rows_per_box != prefill_wide_rows_per_box(p.block_size))
-    return cudaErrorInvalidValue;
+template <int D>
+cudaError_t launch(const PrefillParams& p, const void* q, const void* k_cache,
+                   const void* v_cache, int64_t total_q, int num_kv_heads, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   {
-    // Q as [total_q][Hq][256]: a box of (64 dims, qpk heads, 128/qpk tokens)
+    // Q as [total_q][Hq][D]: a box of (64 dims, qpk heads, 128/qpk tokens)
     // lands as 128 packed rows (token-major, head-minor) in one panel.
     uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(p.num_q_heads),
                         static_cast<uint64_t>(total_q)};
@@ -638,10 +635,38 @@ cudaError_t launch_prefill_wide(const PrefillParams& p, const void* q, const voi
                            p.rows_per_box, true);
   if (e != cudaSuccess) return e;
   static std::atomic<uint64_t> smem_set{0};
-  e = set_smem_once(prefill_wide_kernel, kAlloc, smem_set);
+  e = set_smem_once(prefill_wide_kernel<D>, Geo<D>::kAlloc, smem_set);
   if (e != cudaSuccess) return e;
-  prefill_wide_kernel<<<p.num_ctas, kThreads, kAlloc, stream>>>(mq, mk, mv, p);
+  prefill_wide_kernel<D><<<p.num_ctas, kThreads, Geo<D>::kAlloc, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
+}
+
+
+}  // namespace wide
+}  // namespace
+
+bool prefill_wide_supported(int kv_dtype, int qpk, int block_size) {
+  return kv_dtype == UA_KV_BF16 && qpk >= 1 && qpk <= wide::kRows && wide::kRows % qpk == 0 &&
+         block_size >= 16 && (wide::kKeys % block_size == 0 || block_size % wide::kKeys == 0);
+}
+
+bool prefill_is_wide(int head_dim) { return head_dim == 192 || head_dim == 256; }
+
+int prefill_wide_rows_per_box(int block_size) {
+  return block_size < wide::kKeys ? block_size : wide::kKeys;
+}
+
+cudaError_t launch_prefill_wide(const PrefillParams& p, const void* q, const void* k_cache,
+                                const void* v_cache, int64_t total_q, int head_dim,
+                                int num_kv_heads, cudaStream_t stream) {
+  if (p.num_tiles <= 0 || p.num_ctas <= 0) return cudaSuccess;
+  if (p.counters == nullptr || p.rows_per_box != prefill_wide_rows_per_box(p.block_size))
+    return cudaErrorInvalidValue;
+  switch (head_dim) {
+    case 192: return wide::launch<192>(p, q, k_cache, v_cache, total_q, num_kv_heads, stream);
+    case 256: return wide::launch<256>(p, q, k_cache, v_cache, total_q, num_kv_heads, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace ua

@@ -156,7 +156,7 @@ extern "C" ua_status ua_forward_static_scratch(
     return UA_ERR_INVALID_ARG;
   if (num_q_heads % num_kv_heads != 0) return UA_ERR_INVALID_ARG;
   if (kv_dtype != UA_KV_BF16 && kv_dtype != UA_KV_FP8_E4M3) return UA_ERR_INVALID_ARG;
-  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return UA_ERR_UNSUPPORTED;
+  if (head_dim < 32 || head_dim > 256 || head_dim % 32 != 0) return UA_ERR_UNSUPPORTED;
   if (block_size % 16 != 0) return UA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size < max_kv) return UA_ERR_INVALID_ARG;
   if (num_seqs == 0 || max_q == 0) return UA_OK;

@@ -581,7 +581,7 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     pp.window = plan->prob.window;
     pp.score_scale_log2 = kp.score_scale_log2;
     pp.out_scale = kp.v_scale;
-    const bool wide = plan->prob.head_dim == 256;
+    const bool wide = ua::prefill_is_wide(plan->prob.head_dim);
     pp.rows_per_box = wide ? ua::prefill_wide_rows_per_box(pp.block_size)
                            : (pp.block_size < 128 ? pp.block_size : 128);
     pp.timeout_ns = plan->wait_timeout_ns;
@@ -593,7 +593,8 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     if (mixed) span_begin(mp, 0, &pp.span_start, &pp.span_end);
     else ev = timing_begin(mp, 0, cs);
     const cudaError_t le =
-        wide ? ua::launch_prefill_wide(pp, q, pk, pv, plan->total_q, plan->prob.num_kv_heads, cs)
+        wide ? ua::launch_prefill_wide(pp, q, pk, pv, plan->total_q, plan->prob.head_dim,
+                                       plan->prob.num_kv_heads, cs)
              : ua::launch_prefill(pp, q, pk, pv, plan->total_q, plan->prob.head_dim,
                                   plan->prob.num_kv_heads, cs);
     if (le != cudaSuccess) return UA_ERR_CUDA;

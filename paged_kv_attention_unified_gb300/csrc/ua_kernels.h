@@ -70,15 +70,16 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_
                            const void* v_cache, int64_t total_q, int head_dim,
                            int num_kv_heads, cudaStream_t stream);
 
-// head_dim 256 prefill kernel (one 128-row query tile at a time, 64-key
-// tiles): whether it takes the problem, the keys per TMA box it needs
+// head_dim 192 / 256 prefill kernel (one 128-row query tile at a time,
+// 64-key tiles): whether it takes the problem, the keys per TMA box it needs
 // (PrefillParams::rows_per_box), and its launch (same parameters as
 // launch_prefill).
 bool prefill_wide_supported(int kv_dtype, int qpk, int block_size);
 int prefill_wide_rows_per_box(int block_size);
+bool prefill_is_wide(int head_dim);
 cudaError_t launch_prefill_wide(const PrefillParams& p, const void* q, const void* k_cache,
-                                const void* v_cache, int64_t total_q, int num_kv_heads,
-                                cudaStream_t stream);
+                                const void* v_cache, int64_t total_q, int head_dim,
+                                int num_kv_heads, cudaStream_t stream);
 
 // Tensor map of a row-major tensor (dims innermost first, strides in bytes of
 // dims 1..rank-1) for bf16 (elt_bytes 2) or byte (elt_bytes 1) elements;

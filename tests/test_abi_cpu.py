@@ -63,7 +63,7 @@ def test_invalid_problems_are_rejected(bad):
     assert e.value.status == ua.UA_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("d,bs", [(96, 16), (128, 8), (512, 16), (32, 16), (64, 24)])
+@pytest.mark.parametrize("d,bs", [(80, 16), (128, 8), (512, 16), (16, 16), (288, 16), (64, 24)])
 def test_unsupported_shapes(d, bs):
     with pytest.raises(ua.UAError) as e:
         ua.ua_schedule([0, 1], [5], 4, 4, d, bs, 64)
@@ -95,9 +95,9 @@ def _check_schedule(cu, kv, hq, hkv, causal=1, window=0, num_splits=0, num_sms=1
                                          causal=causal, window=window, num_splits=num_splits,
                                          num_sms=num_sms, decode_rows_max=decode_rows_max)
     qpk = hq // hkv
-    # the prefill kernel takes bf16 caches with qpk dividing 128 (block size 16
-    # here) at head_dim 64 and 128
-    prefill_ok = 128 % qpk == 0 and d in (64, 128)
+    # the prefill kernels take bf16 caches with qpk dividing 128 (block size 16
+    # here) at head_dim 64, 128, 192 and 256
+    prefill_ok = 128 % qpk == 0 and d in (64, 128, 192, 256)
     rows_max = (2 ** 63) if not prefill_ok else (32 if decode_rows_max < 0 else decode_rows_max)
     seen = {}
     for kind, tiles, rows_per in (("pre", pre, ua.UA_PREFILL_ROWS), ("dec", dec, 8)):

@@ -252,6 +252,49 @@ def test_head_dim_256_allocation_free_entry_point_matches_oracle():
     assert_close(as_f64(out), oracle_full(case), case.kv_dtype, case.name)
 
 
+# ---- every other head_dim that is a multiple of 32 up to 256: the decode
+# kernel (and at 192 the wide prefill kernel for long prefills)
+
+NEW_DIMS = [32, 96, 160, 192, 224]
+
+
+@pytest.mark.parametrize("dtype", [W.BF16, W.FP8])
+@pytest.mark.parametrize("d", NEW_DIMS)
+def test_other_head_dims_random(d, dtype):
+    for seed in (800, 801):
+        _check(W.random_small_case(seed + d, kv_dtype=dtype, head_dim=d, num_q_heads=8,
+                                   num_kv_heads=2, max_kv=700))
+
+
+@pytest.mark.parametrize("d", NEW_DIMS)
+def test_other_head_dims_splits_window_noncausal_and_poison(d):
+    _check(W.make_case(f"d{d}_split", [1, 1, 3, 1], [3000, 70, 1300, 16], 16, 4, d, 16,
+                       seed=810 + d), num_splits=7)
+    _check(W.make_case(f"d{d}_win", [1, 40], [2000, 600], 8, 2, d, 32, window=300,
+                       seed=811 + d))
+    _check(W.make_case(f"d{d}_nc", [1, 30], [900, 300], 4, 4, d, 16, causal=False,
+                       seed=812 + d))
+    _check(W.make_case(f"d{d}_fp8", [1, 3], [4000, 900], 16, 2, d, 16, kv_dtype=W.FP8,
+                       poison=True, seed=813 + d), num_splits=16)
+
+
+@pytest.mark.parametrize("d", [96, 160])
+def test_other_head_dims_allocation_free_entry_point(d):
+    case = W.make_case(f"d{d}_static", [1, 1, 1, 1], [3000, 70, 1200, 16], 8, 2, d, 16,
+                       seed=830 + d)
+    b = tu.to_device(case)
+    out = b.new_out()
+    err = torch.full((1,), -99, dtype=torch.int32, device="cuda")
+    ua.ua_forward_static_scratch(
+        b.q, b.k_cache, b.v_cache, out, b.cu_query_lens, b.kv_lens, b.block_tables,
+        b.num_q_heads, b.num_kv_heads, b.head_dim, b.block_size, int(b.block_tables.shape[1]),
+        b.num_blocks, b.kv_dtype, b.max_q, b.max_kv, b.scale, causal=b.causal, window=b.window,
+        k_scale=b.k_scale, v_scale=b.v_scale, num_splits=4, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(as_f64(out), oracle_full(case), case.kv_dtype, case.name)
+
+
 def test_plan_churn_reuses_pooled_memory():
     """A serving loop builds and drops a plan every step: plan memory comes
     from the library's stream-ordered pool and pinned upload blocks, so 200

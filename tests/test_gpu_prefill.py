@@ -238,7 +238,7 @@ def test_many_ragged_sequences_through_both_kernels():
     assert_close(as_f64(out), oracle_full_parallel(case), case.kv_dtype, case.name, report=True)
 
 
-# ---- head_dim 256: the wide prefill kernel (one 128-row query tile, 64-key tiles)
+# ---- head_dim 192 / 256: the wide prefill kernel (one 128-row query tile, 64-key tiles)
 
 def _check_wide(case, decode_rows_max=0):
     b = tu.to_device(case)
@@ -250,24 +250,26 @@ def _check_wide(case, decode_rows_max=0):
     return assert_close(as_f64(out), oracle_full(case), case.kv_dtype, case.name)
 
 
+@pytest.mark.parametrize("d", [192, 256])
 @pytest.mark.parametrize("qpk,hkv,bs", [(1, 2, 16), (2, 2, 32), (4, 1, 64), (8, 1, 128),
                                         (4, 2, 16)])
-def test_wide_prefill_matches_oracle(qpk, hkv, bs):
+def test_wide_prefill_matches_oracle(qpk, hkv, bs, d):
     """Ragged prefills with contexts that are not multiples of 16 or 64, and a
     query tile that straddles the 128-row item boundary."""
-    _check_wide(W.make_case(f"wide_{qpk}_{bs}", [300, 77, 129, 1], [300, 533, 200, 90],
-                            qpk * hkv, hkv, 256, bs, seed=700 + bs + qpk))
+    _check_wide(W.make_case(f"wide_d{d}_{qpk}_{bs}", [300, 77, 129, 1], [300, 533, 200, 90],
+                            qpk * hkv, hkv, d, bs, seed=700 + bs + qpk + d))
 
 
-def test_wide_prefill_window_noncausal_poison_and_fp8():
-    _check_wide(W.make_case("wide_win", [400, 260], [900, 260], 8, 2, 256, 16, window=150,
-                            seed=710))
-    _check_wide(W.make_case("wide_nc", [200, 90], [600, 90], 8, 2, 256, 32, causal=False,
-                            seed=711))
-    _check_wide(W.make_case("wide_poison", [333, 150], [700, 181], 8, 2, 256, 16, poison=True,
-                            seed=712))
-    _check_wide(W.make_case("wide_fp8", [300, 77, 150], [300, 500, 460], 8, 2, 256, 16,
-                            kv_dtype=W.FP8, seed=713))
+@pytest.mark.parametrize("d", [192, 256])
+def test_wide_prefill_window_noncausal_poison_and_fp8(d):
+    _check_wide(W.make_case("wide_win", [400, 260], [900, 260], 8, 2, d, 16, window=150,
+                            seed=710 + d))
+    _check_wide(W.make_case("wide_nc", [200, 90], [600, 90], 8, 2, d, 32, causal=False,
+                            seed=711 + d))
+    _check_wide(W.make_case("wide_poison", [333, 150], [700, 181], 8, 2, d, 16, poison=True,
+                            seed=712 + d))
+    _check_wide(W.make_case("wide_fp8", [300, 77, 150], [300, 500, 460], 8, 2, d, 16,
+                            kv_dtype=W.FP8, seed=713 + d))
 
 
 def test_wide_prefill_mixed_with_decode_and_repeated():
@@ -325,7 +327,7 @@ def test_full_size_wide_dense_prefill_whole_output_and_first_row_exact():
                  f"workload 9 ({case.name})", report=True)
 
 
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [128, 192, 256])
 def test_one_persistent_cta_runs_every_tile_in_turn(d):
     """One prefill CTA takes every work tile of the batch in sequence, so every
     barrier phase, ring position and TMEM buffer runs on across many tiles
