@@ -28,8 +28,15 @@ are widened to fp64 exactly from their format definitions.
 The append step (writing a step's new K/V into the paged cache, with the
 e4m3 quantisation of the fp8 cache) is in oracle/append.py.
 
-Parity pins live in tests/test_oracle_pins.py and tests/test_append_pins.py;
-every function is pinned there (none is "parity unpinned").
+The fp8-products variant (fp8 Q.K^T and fp8 P, the FP8 path of the "Fused
+Attention" notes) is in oracle/fp8_products.py. There the key blocks and the
+running max are part of what the method computes -- P is rounded to e4m3
+relative to the running max of its block -- so that oracle follows the
+blockwise recurrence, still in binary64.
+
+Parity pins live in tests/test_oracle_pins.py, tests/test_append_pins.py and
+tests/test_fp8_products_pins.py; every function is pinned there (none is
+"parity unpinned").
 """
 from .attention import (  # noqa: F401
     decode_bf16,
@@ -44,3 +51,9 @@ from .attention import (  # noqa: F401
     combine_partials,
 )
 from .append import encode_e4m3, quantize_e4m3, append_kv  # noqa: F401
+from .fp8_products import (  # noqa: F401
+    round_e4m3,
+    quantize_q_rows,
+    attend_fp8_blocks,
+    paged_attention_fp8_products,
+)
