@@ -370,6 +370,12 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
     plan.set_unified_max(args.unified_max)
     if args.prefill_ctas:
         ua.ua_plan_set_prefill_ctas(plan.handle, args.prefill_ctas)
+    f8p = bool(getattr(args, "fp8_products", False)) and case.kv_dtype == "fp8_e4m3"
+    if f8p:
+        ua.ua_plan_set_fp8_products(plan.handle, True)
+        # e4m3 operands: the fp8 dense peak, the measured bf16 one times the
+        # nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+        tf_peak *= 2.0
     info = plan.info
     out = b.new_out()
     stream = torch.cuda.current_stream()
@@ -448,6 +454,8 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
                  "frac": ach / hbm_peak, "work_per_launch": k_bytes}
         r["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" \
             if peak_src == "measured" else "fallback"
+        if f8p and kind == "prefill":
+            r["peak_source"] += " x 2 (e4m3 operands: nominal fp8 / bf16 dense ratio)"
         r["kernel"] = kind
         r["kernel_avg_us"] = avg_s * 1e6
         r["kernel_share"] = kms / max(1e-9, sum(v[0] for v in ktimes.values()))
@@ -507,8 +515,9 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
                "includes": "one ua_forward_host call per step: CPU scheduling, one upload of "
                            "tiles + lengths + page tables, H2D of q, forward, D2H of the output "
                            "and the error word, stream synchronisation (pinned host buffers)"}
-        if args.unified_max is not None or args.prefill_ctas:
-            e2e["note"] = "the scheduler's default settings (no unified max / CTA override)"
+        if args.unified_max is not None or args.prefill_ctas or f8p:
+            e2e["note"] = ("the one-call entry point's default settings (no unified max / CTA "
+                           "override / fp8 products)")
     plan.close()
     l2_note = ("inputs larger than L2 (%.2f GB > 0.129 GB)" % (byts / 1e9)) if flush is None \
         else "L2 flushed (256 MB write) between timed steps"
@@ -520,7 +529,8 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
         "sustained": {"value": _rate(cfg, job_bytes, job_flops, soak_max / 1e3),
                       "ms_per_step": soak_max, "steps": soak_n, "seconds": soak_ms / 1e3}
         if soak_n else None,
-        "dtype": _dtype_for(case),
+        "dtype": "e4m3 Q, K, V, P operands (kind::f8f6f4), fp32 accumulate" if f8p
+                 else _dtype_for(case),
         "l2": l2_note,
         "tiles": {"decode": info.num_decode_tiles, "prefill": info.num_prefill_tiles,
                   "split_tokens": info.split_tokens,
@@ -550,7 +560,7 @@ def run_ours(args):
     head = measure_attention(cfg, args, rank, world, with_cpu, args.soak, args.cpu_budget)
     if args.per_config == "auto":
         extra = [3, 4, 5] if cfg == 2 and not args.window and not args.num_splits and \
-            args.unified_max is None and not args.prefill_ctas else []
+            args.unified_max is None and not args.prefill_ctas and not args.fp8_products else []
     elif args.per_config in ("", "none"):
         extra = []
     else:
@@ -577,7 +587,8 @@ def run_ours(args):
                    "prefill_ctas": head["tiles"]["prefill_ctas"],
                    **({"unified_max": args.unified_max} if args.unified_max is not None else {}),
                    **({"num_splits": args.num_splits} if args.num_splits else {}),
-                   **({"window": args.window} if args.window else {})},
+                   **({"window": args.window} if args.window else {}),
+                   **({"fp8_products": True} if args.fp8_products else {})},
         "algorithmic": head["algorithmic"], "pct_of_peak": head["pct_of_peak"],
         "sustained": head["sustained"], "roofline": head["roofline"],
         "step_roofline": head["step_roofline"], "cpu_baseline": head["cpu_baseline"],
@@ -806,6 +817,9 @@ def main():
                     help="left sliding window of W keys for the attention step (0: none)")
     ap.add_argument("--num-splits", type=int, default=0, metavar="N",
                     help="cut every decode tile into N split pieces (0: automatic sizing)")
+    ap.add_argument("--fp8-products", action="store_true",
+                    help="fp8 cache workloads: prefill tiles with e4m3 tensor-core products "
+                         "(ua_plan_set_fp8_products)")
     ap.add_argument("--prefill-ctas", type=int, default=0, metavar="P",
                     help="persistent prefill CTAs of a mixed step (0: the scheduler's choice)")
     ap.add_argument("--unified-max", type=float, default=None, metavar="PHI",

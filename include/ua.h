@@ -350,6 +350,23 @@ ua_status ua_plan_set_unified_max(ua_plan* plan, int32_t enable, float phi);
  * do not depend on it. */
 ua_status ua_plan_set_prefill_ctas(ua_plan* plan, int32_t num_ctas);
 
+/* fp8 tensor-core products for the prefill tiles of an fp8 (e4m3) cache:
+ * the low-precision path of the "Fused Attention" notes (Q.K^T on fp8
+ * operands, P cast to fp8 ahead of P.V; the block-quantised FP8 path of
+ * their FlashAttention-3 summary). With enable = 1, later ua_forward calls
+ * run the prefill tiles in a kernel that reads the e4m3 cache directly (no
+ * bf16 staging copy): each query row is quantised to e4m3 with its own scale
+ * (448 / max |q|, binary32), S = Q K^T and O += P V are kind::f8f6f4 MMAs,
+ * and P (exp relative to the row's running max, <= 1) is rounded to e4m3,
+ * while l sums the unrounded P. Accuracy is that of the fp8 operands
+ * (about 2^-4 relative per element) rather than of the exact dequantised
+ * cache; decode tiles keep their f16 products. enable = 0 restores the
+ * staged path. Returns UA_ERR_UNSUPPORTED unless the plan has an e4m3 cache,
+ * head_dim 128, 128 % qpk == 0 and a block size that divides or is divided
+ * by 128 (and at least 16); UA_ERR_INVALID_ARG for a null plan or an enable
+ * other than 0 / 1. */
+ua_status ua_plan_set_fp8_products(ua_plan* plan, int32_t enable);
+
 /* Synchronises the plan's last stream, reads the device error word
  * (UA_OK, UA_ERR_BOUNDS or UA_ERR_DEVICE_TIMEOUT) into *code and clears it. */
 ua_status ua_last_device_error(ua_plan* plan, int32_t* code);

@@ -16,19 +16,24 @@ Hopper. Over a paged e4m3 cache with per-tensor scales k_scale, v_scale:
      (k8 the cache's e4m3 values), exactly as in the bf16 definition
      otherwise (causal / window / key range).
   3. online softmax over key blocks of BLOCK_N = 128 keys aligned to multiples
-     of 128 (the blocks of the tutorial's inner loop): per block the running
-     max m_b = max(m_{b-1}, max s over the block), alpha = exp(m_{b-1} - m_b),
-     p = exp(s - m_b) over the block, l = l * alpha + sum p (from p before
-     the cast, as the tutorial sums p ahead of `p.to(dtype)`), and
+     of 128 (the blocks of the tutorial's inner loop), against a reference
+     m_b that follows the running max lazily: m_b = max(m_{b-1}, max s over
+     the block) when that exceeds m_{b-1} by more than 8 ln 2 (or m_{b-1} is
+     -inf), else m_b = m_{b-1}; alpha = exp(m_{b-1} - m_b), p = exp(s - m_b)
+     over the block (so p <= 2^8), l = l * alpha + sum p (from p before the
+     cast, as the tutorial sums p ahead of `p.to(dtype)`), and
      acc = acc * alpha + e4m3(p) . v8 (p rounded to e4m3, nearest even).
   4. out = acc * v_scale / l (rows with no visible key: 0).
 
 Readings (where the pages leave the step open): one quantisation scale per
 query row (the finest "block" of the block quantisation, and exact for the
-largest element of every row); P cast to e4m3 as it stands, P <= 1, without a
-scale (the tutorial casts p as it stands; e4m3 keeps values down to 2^-9, so
-weights below about 2^-10 of the row's running max drop out); l from the
-unrounded p (the tutorial's l_ij is the sum of p before the cast).
+largest element of every row); P cast to e4m3 as it stands (the tutorial
+casts p as it stands), against a reference that moves only when the row max
+has grown by more than 2^8: the exact-max recurrence of the tutorial gives
+the same softmax, and a lagging reference keeps p within [0, 2^8], inside
+e4m3's range (448), while weights down to 2^-10 of the reference survive
+the cast (e4m3 keeps values down to 2^-9); l from the unrounded p (the
+tutorial's l_ij is the sum of p before the cast).
 
 Everything is in binary64 except the two quantisation decisions, which take
 the binary32 values the GPU path also rounds.
@@ -43,6 +48,9 @@ from .attention import FP8, decode_bf16, gather_kv, kv_head_of, visible_keys
 
 BLOCK_N = 128
 E4M3_MAX = 448.0
+# The reference max moves when the block max exceeds it by more than this
+# (natural-log units; 8 in log2 units).
+LAG = 8.0 * np.log(2.0)
 
 
 def round_e4m3(x: np.ndarray) -> np.ndarray:
@@ -97,7 +105,10 @@ def attend_fp8_blocks(q8: np.ndarray, inv: np.ndarray, K8: np.ndarray, V8: np.nd
         mask = vis[:, cols]
         sb = np.where(mask, S[:, cols], -np.inf)
         bmax = np.max(sb, axis=1)
-        m_new = np.maximum(m, bmax)
+        m_max = np.maximum(m, bmax)
+        with np.errstate(invalid="ignore"):
+            grow = ~np.isfinite(m) | (m_max > m + LAG)
+        m_new = np.where(grow, m_max, m)
         live = np.isfinite(m_new)
         with np.errstate(invalid="ignore"):
             alpha = np.where(live & np.isfinite(m), np.exp(m - m_new), 0.0)

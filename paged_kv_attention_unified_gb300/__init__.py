@@ -34,7 +34,7 @@ EXPORTS = (
     "ua_plan_get_info", "ua_last_device_error", "ua_plan_destroy", "ua_status_string",
     "ua_gather_kv_debug", "ua_plan_set_profiling", "ua_plan_kernel_times",
     "ua_forward_static_scratch", "ua_plan_set_debug", "ua_append_kv",
-    "ua_plan_set_unified_max", "ua_plan_set_prefill_ctas", "ua_forward_host",
+    "ua_plan_set_unified_max", "ua_plan_set_prefill_ctas", "ua_plan_set_fp8_products", "ua_forward_host",
 )
 
 
@@ -95,6 +95,7 @@ _SIGS = {
     "ua_plan_set_debug": (_I32, [_P, _I32, _I64]),
     "ua_plan_set_unified_max": (_I32, [_P, _I32, _F]),
     "ua_plan_set_prefill_ctas": (_I32, [_P, _I32]),
+    "ua_plan_set_fp8_products": (_I32, [_P, _I32]),
     "ua_forward_static_scratch": (_I32, [_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32,
                                          _I32, _I32, _I64, _I32, _I32, _I32, _F, _I32, _I32, _F,
                                          _F, _I32, _P, _P]),
@@ -273,6 +274,12 @@ def ua_plan_set_debug(plan: int, flags: int, wait_timeout_ns: int = 0):
 def ua_plan_set_prefill_ctas(plan: int, num_ctas: int = 0):
     """Prefill CTAs of later forwards on this plan (0: the scheduler's count)."""
     _check(lib().ua_plan_set_prefill_ctas(plan, int(num_ctas)), "ua_plan_set_prefill_ctas")
+
+
+def ua_plan_set_fp8_products(plan: int, enable: bool = True):
+    """fp8 tensor-core products for the prefill tiles of an e4m3 cache (later
+    forwards on this plan); enable=False restores the staged bf16 path."""
+    _check(lib().ua_plan_set_fp8_products(plan, 1 if enable else 0), "ua_plan_set_fp8_products")
 
 
 def ua_plan_set_unified_max(plan: int, phi=None):

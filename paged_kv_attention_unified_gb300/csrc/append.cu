@@ -30,18 +30,6 @@ constexpr int kWarpsPerCta = 8;   // tokens per append tile (one warp each)
 constexpr int kUnroll = 4;        // 16-byte chunks per lane in flight (rows up to 4 KB of bf16)
 static_assert(kWarpsPerCta == kAppendTokens, "one warp per token of an append tile");
 
-// Four binary32 values -> four e4m3 codes (x0 in the lowest byte).
-__device__ __forceinline__ uint32_t to_e4m3x4(float x0, float x1, float x2, float x3) {
-  uint16_t lo, hi;
-  // the first source operand lands in the upper byte of the pair
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
-  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
-  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
 // Eight bf16 values (one 16-byte chunk) / scale -> eight e4m3 codes.
 __device__ __forceinline__ uint2 quantize8(uint4 w, float scale) {
   const float a0 = __fdiv_rn(bf16_lo(w.x), scale), a1 = __fdiv_rn(bf16_hi(w.x), scale);

@@ -65,12 +65,19 @@ constexpr int kItemBytes = 64;  // one descriptor in shared memory
 // thread and the eight softmax warps (one lane each).
 constexpr int kItemConsumers = 3 + 8;
 
-template <int D>
+// F8: the fp8-products variant (e4m3 Q, K, V and P operands of kind::f8f6f4
+// MMAs over an e4m3 cache, head_dim 128): 1-byte elements, so one 128-byte
+// swizzled panel holds a whole 128-wide row.
+template <int D, bool F8>
 struct Smem {
-  static constexpr int kKStages = D == 128 ? 3 : 4;
-  static constexpr int kVStages = D == 128 ? 2 : 4;
-  static constexpr int kPanel = kRows * 128;           // one 64-wide bf16 panel: 16 KB
-  static constexpr int kTile = kRows * D * 2;           // 128 x D bf16
+  static_assert(!F8 || D == 128, "fp8 products at head_dim 128");
+  static constexpr int kElt = F8 ? 1 : 2;                // operand bytes
+  static constexpr int kPanelDims = 128 / kElt;          // head dims per 128-byte panel
+  static constexpr int kPanels = D / kPanelDims;
+  static constexpr int kKStages = F8 ? 4 : (D == 128 ? 3 : 4);
+  static constexpr int kVStages = F8 ? 4 : (D == 128 ? 2 : 4);
+  static constexpr int kPanel = kRows * 128;            // one panel of 128 rows: 16 KB
+  static constexpr int kTile = kRows * D * kElt;        // 128 x D operands
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kTilesPerCta * kTile;
   static constexpr int kV = kK + kKStages * kTile;
@@ -87,9 +94,9 @@ struct Smem {
 
 // The CTA's mbarriers as 32-bit shared-window addresses: one base register
 // and constant offsets (8 bytes per barrier).
-template <int D>
+template <int D, bool F8>
 struct Bars {
-  static constexpr int KS = Smem<D>::kKStages, VS = Smem<D>::kVStages;
+  static constexpr int KS = Smem<D, F8>::kKStages, VS = Smem<D, F8>::kVStages;
   uint32_t base;
   __device__ __forceinline__ uint32_t at(int i) const { return base + 8u * static_cast<uint32_t>(i); }
   __device__ __forceinline__ uint32_t q_full(int t) const { return at(t); }   // Q of query tile t landed
@@ -181,8 +188,8 @@ __device__ __forceinline__ void give_up(const PrefillParams& p, volatile int32_t
 // empty it publishes an end marker. The last CTA to finish (p.counters[1])
 // resets both counters for the next launch; a CTA that gives up still counts
 // itself, so the reset happens on the error path too.
-template <int D>
-__device__ __forceinline__ void scheduler_role(const PrefillParams& p, const Bars<D>& bar,
+template <int D, bool F8>
+__device__ __forceinline__ void scheduler_role(const PrefillParams& p, const Bars<D, F8>& bar,
                                                uint8_t* ring, volatile int32_t* abort) {
   for (int k = 0;; ++k) {
     const int s = k % kItemSlots;
@@ -214,8 +221,8 @@ __device__ __forceinline__ void scheduler_role(const PrefillParams& p, const Bar
 
 // Wait for work-tile descriptor k and copy it out of the ring. The caller
 // then frees the slot (one arrival per consumer thread or softmax warp).
-template <int D>
-__device__ __forceinline__ bool take_item(const PrefillParams& p, const Bars<D>& bar,
+template <int D, bool F8>
+__device__ __forceinline__ bool take_item(const PrefillParams& p, const Bars<D, F8>& bar,
                                           const uint8_t* ring, int k, Item& it,
                                           volatile int32_t* abort) {
   const int s = k % kItemSlots;
@@ -229,15 +236,15 @@ __device__ __forceinline__ bool take_item(const PrefillParams& p, const Bars<D>&
 // 128 rows of a larger page) and 64-wide panel. Every page id is read from
 // the block table and checked; a missing or out-of-range page is loaded from
 // an out-of-range block coordinate, which TMA fills with zeros.
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ void load_key_tile(const CUtensorMap* map, const PrefillParams& p,
                                               const Item& tile, const Geometry& g, int j,
                                               uint8_t* dst, uint32_t full) {
-  using L = Smem<D>;
-  constexpr int kPanels = D / 64;
+  using L = Smem<D, F8>;
+  constexpr int kPanels = L::kPanels;
   const int boxes = kKeys / p.rows_per_box;
   const int base = g.kv_lo + j * kKeys;
-  mbar_arrive_expect_tx(full, kKeys * D * 2);
+  mbar_arrive_expect_tx(full, L::kTile);
   for (int b = 0; b < boxes; ++b) {
     const int key0 = base + b * p.rows_per_box;
     int32_t blk = static_cast<int32_t>(p.num_blocks);  // out of range: zero fill
@@ -255,7 +262,8 @@ __device__ __forceinline__ void load_key_tile(const CUtensorMap* map, const Pref
     const int row_off = b * p.rows_per_box * 128;
 #pragma unroll
     for (int pn = 0; pn < kPanels; ++pn)
-      tma_load_4d(dst + pn * L::kPanel + row_off, map, full, pn * 64, tile.kv_head, slot, blk);
+      tma_load_4d(dst + pn * L::kPanel + row_off, map, full, pn * L::kPanelDims, tile.kv_head,
+                  slot, blk);
   }
 }
 
@@ -263,17 +271,17 @@ __device__ __forceinline__ void load_key_tile(const CUtensorMap* map, const Pref
 // of query tile 1 after the first key tile (a Q buffer is refilled once the
 // last S MMA of the previous work tile has read it). One thread of warp 2
 // (kIsV): the V ring. Ring positions run on across the CTA's work tiles.
-template <int D, bool kIsV>
+template <int D, bool F8, bool kIsV>
 __device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CUtensorMap* map_kv,
                                               const PrefillParams& p, const uint8_t* ring,
                                               uint8_t* sQ, uint8_t* sRing, uint32_t full,
-                                              uint32_t empty, const Bars<D>& bar,
+                                              uint32_t empty, const Bars<D, F8>& bar,
                                               volatile int32_t* abort, volatile int32_t* never) {
-  using L = Smem<D>;
-  constexpr int kPanels = D / 64;
+  using L = Smem<D, F8>;
+  constexpr int kPanels = L::kPanels;
   constexpr int kStages = kIsV ? L::kVStages : L::kKStages;
   prefetch_tmap(map_kv);
-  if (!kIsV) prefetch_tmap(map_q);
+  if (!kIsV && !F8) prefetch_tmap(map_q);
   const bool idle = (p.debug_flags & kDebugProducerIdle) != 0;
   int last_phase[kStages];
 #pragma unroll
@@ -282,7 +290,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CU
   bool ok = true;
   // Q of query tile t is loaded exactly when the MMA issuer will consume it.
   auto load_q = [&](const Item& tile, const Geometry& g, int t) {
-    if (g.ntiles[t] <= 0) return true;
+    if (F8 || g.ntiles[t] <= 0) return true;  // F8: the softmax warps write Q
     if (q_loads[t] > 0 &&
         !mbar_wait(bar.q_empty(t), (q_loads[t] - 1) & 1, abort, p.timeout_ns))
       return false;
@@ -298,7 +306,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CU
     int step = 0;  // position in the ring sequence
     for (int k = 0; ok; ++k) {
       Item tile;
-      if (!take_item<D>(p, bar, ring, k, tile, abort)) {
+      if (!take_item<D, F8>(p, bar, ring, k, tile, abort)) {
         ok = false;
         break;
       }
@@ -314,7 +322,7 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CU
           ok = false;
           break;
         }
-        load_key_tile<D>(map_kv, p, tile, g, j, sRing + s * L::kTile, full + 8u * s);
+        load_key_tile<D, F8>(map_kv, p, tile, g, j, sRing + s * L::kTile, full + 8u * s);
         last_phase[s] = step / kStages;
         if (!kIsV && j == 0) ok = load_q(tile, g, 1);
       }
@@ -337,15 +345,19 @@ __device__ __forceinline__ void producer_role(const CUtensorMap* map_q, const CU
 // ------------------------------------------------------------------ MMA issuer
 // Per work tile: S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...; ring
 // positions and the per-query-tile barrier phases run on across work tiles.
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ void mma_role(const PrefillParams& p, const uint8_t* ring, uint8_t* sQ,
                                          uint8_t* sK, uint8_t* sV, uint32_t tmem,
-                                         const Bars<D>& bar, volatile int32_t* abort,
+                                         const Bars<D, F8>& bar, volatile int32_t* abort,
                                          volatile int32_t* never) {
-  using L = Smem<D>;
+  using L = Smem<D, F8>;
   constexpr int KS = L::kKStages, VS = L::kVStages;
-  constexpr uint32_t idesc_s = idesc_bf16_f32(kRows, kKeys, 0, 0);
-  constexpr uint32_t idesc_o = idesc_bf16_f32(kRows, D, 0, 1);
+  constexpr uint32_t idesc_s =
+      F8 ? idesc_e4m3_f32(kRows, kKeys, 0, 0) : idesc_bf16_f32(kRows, kKeys, 0, 0);
+  constexpr uint32_t idesc_o = F8 ? idesc_e4m3_f32(kRows, D, 0, 1) : idesc_bf16_f32(kRows, D, 0, 1);
+  // One MMA covers kStep elements of the contraction: 32 bytes of every
+  // operand row (16 bf16 or 32 e4m3 values).
+  constexpr int kStep = 32 / L::kElt;
   // Each operand descriptor is built once per group of MMAs; the k-th MMA
   // adds its byte offset / 16 to the 14-bit start-address field (shared
   // addresses stay below 256 KB, so the field cannot overflow).
@@ -353,18 +365,27 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, const uint8_t* 
     const uint64_t qd = smem_desc_sw128(opaque_u32(smem_u32(sQ)) + t * L::kTile, 16, 1024);
     const uint64_t kd = smem_desc_sw128(smem_u32(sK) + (gj % KS) * L::kTile, 16, 1024);
 #pragma unroll
-    for (int k = 0; k < D / 16; ++k) {
+    for (int k = 0; k < D / kStep; ++k) {
       const uint64_t off = static_cast<uint64_t>(((k / 4) * L::kPanel + (k % 4) * 32) >> 4);
-      mma_ss(tmem + t * kKeys, qd + off, kd + off, idesc_s, k > 0 ? 1u : 0u);
+      if constexpr (F8) mma_ss_f8(tmem + t * kKeys, qd + off, kd + off, idesc_s, k > 0 ? 1u : 0u);
+      else mma_ss(tmem + t * kKeys, qd + off, kd + off, idesc_s, k > 0 ? 1u : 0u);
     }
     mma_commit(bar.s_full(t));
   };
+  // P from TMEM (kStep keys = 8 columns per MMA), V's rows kStep * 128 bytes
+  // apart per MMA.
   auto issue_pv = [&](int t, int gj, bool acc) {
     const uint64_t vd = smem_desc_sw128(smem_u32(sV) + (gj % VS) * L::kTile, L::kPanel, 1024);
 #pragma unroll
-    for (int k = 0; k < kKeys / 16; ++k)
-      mma_ts(tmem + 256 + t * 128, tmem + t * kKeys + 8 * k,
-             vd + static_cast<uint64_t>((k * 2048) >> 4), idesc_o, (acc || k > 0) ? 1u : 0u);
+    for (int k = 0; k < kKeys / kStep; ++k) {
+      const uint64_t off = static_cast<uint64_t>((k * kStep * 128) >> 4);
+      if constexpr (F8)
+        mma_ts_f8(tmem + 256 + t * 128, tmem + t * kKeys + 8 * k, vd + off, idesc_o,
+                  (acc || k > 0) ? 1u : 0u);
+      else
+        mma_ts(tmem + 256 + t * 128, tmem + t * kKeys + 8 * k, vd + off, idesc_o,
+               (acc || k > 0) ? 1u : 0u);
+    }
     mma_commit(bar.o_done(t));
   };
   int step = 0;                       // ring position of key tile 0 of the work tile
@@ -373,7 +394,7 @@ __device__ __forceinline__ void mma_role(const PrefillParams& p, const uint8_t* 
   bool ok = true;
   for (int k = 0; ok; ++k) {
     Item it;
-    if (!take_item<D>(p, bar, ring, k, it, abort)) {
+    if (!take_item<D, F8>(p, bar, ring, k, it, abort)) {
       ok = false;
       break;
     }
@@ -468,13 +489,14 @@ struct SoftmaxTile {
 // only touch TMEM lanes 32 * (warp % 4) .. + 31, which fixes the rows of each
 // warp. `done` is the number of key tiles this query tile has already had in
 // earlier work tiles (barrier phases), `step` the ring position of key tile 0.
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const SoftmaxTile& g, int t,
-                                             int done, int step, uint8_t* sV, uint32_t tmem,
-                                             const Bars<D>& bar, volatile int32_t* abort,
+                                             int done, int step, uint8_t* sQ, uint8_t* sV,
+                                             uint32_t tmem,
+                                             const Bars<D, F8>& bar, volatile int32_t* abort,
                                              int warp, int lane) {
-  using L = Smem<D>;
-  constexpr int kPanels = D / 64;
+  using L = Smem<D, F8>;
+  constexpr int kPanels = L::kPanels;
   constexpr int VS = L::kVStages;
   const int n_t = g.n_t;
   const uint32_t quarter = static_cast<uint32_t>(warp & 3);
@@ -488,7 +510,54 @@ __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const Softm
   // Scores are used as x = s * c with c >= 0: a negative scale flips the sign
   // of the raw scores once, so that the row max is always a max.
   const bool neg = p.score_scale_log2 < 0.f;
-  const float c = neg ? -p.score_scale_log2 : p.score_scale_log2;
+  float c = neg ? -p.score_scale_log2 : p.score_scale_log2;
+  if constexpr (F8) {
+    // This thread's Q row to e4m3 with its own scale (inv = 448 / max |q|,
+    // binary32; 1 for a zero row or a row past the end), written into query
+    // tile t's operand tile in the 128-byte swizzled layout TMA would give it
+    // (16-byte chunk k of row r at chunk k ^ (r % 8)). The previous work
+    // tile's products that read this tile have completed (its last P V did,
+    // before this warp's epilogue). The scores then carry 1 / inv.
+    static_assert(D == 128, "one 128-byte row per query row");
+    uint32_t w[D / 2];
+    if (r < g.rows_t) {
+      const uint4* src = reinterpret_cast<const uint4*>(
+          reinterpret_cast<const uint8_t*>(p.q) +
+          (static_cast<int64_t>(g.q_start + row / p.qpk) * p.num_q_heads + g.kv_head * p.qpk +
+           row % p.qpk) * D * 2);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        const uint4 v = src[i];
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < D / 2; ++i) w[i] = 0u;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < D / 2; ++i)
+      amax = fmax3(amax, fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i])));
+    const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+    uint8_t* qrow = sQ + t * L::kTile + r * 128;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      uint32_t e[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t a = w[8 * k + 2 * i], b = w[8 * k + 2 * i + 1];
+        e[i] = to_e4m3x4(__fmul_rn(bf16_lo(a), inv), __fmul_rn(bf16_hi(a), inv),
+                         __fmul_rn(bf16_lo(b), inv), __fmul_rn(bf16_hi(b), inv));
+      }
+      *reinterpret_cast<uint4*>(qrow + ((k ^ (r & 7)) * 16)) = make_uint4(e[0], e[1], e[2], e[3]);
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(bar.q_full(t));
+    c = __fdiv_rn(c, inv);
+  }
   float m = -INFINITY, l = 0.f;
   for (int j = 0; j < n_t; ++j) {
     if (!__all_sync(0xffffffffu, mbar_wait(bar.s_full(t), (done + j) & 1, abort, p.timeout_ns)))
@@ -540,14 +609,28 @@ __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const Softm
     uint64_t sum2[kAcc / 2];
 #pragma unroll
     for (int a = 0; a < kAcc / 2; ++a) sum2[a] = f2_pack(0.f, 0.f);
-    uint32_t pk[kKeys / 2];
+    // P packed for the P V products: bf16 pairs, or e4m3 quadruples (F8:
+    // p <= 2^8 against the lagging reference, inside e4m3's range; l sums the
+    // unrounded p).
+    constexpr int kPk = F8 ? kKeys / 4 : kKeys / 2;
+    uint32_t pk[kPk];
+    float q0 = 0.f, q1 = 0.f;
 #pragma unroll
     for (int i = 0; i < kKeys / 2; ++i) {
       float e0, e1;
       f2_unpack(f2_fma(f2_pack(x[2 * i], x[2 * i + 1]), c2, nsub2), e0, e1);
       const float p0 = ex2(e0), p1 = ex2(e1);
       sum2[i % (kAcc / 2)] = f2_add(sum2[i % (kAcc / 2)], f2_pack(p0, p1));
-      pk[i] = pack2<false>(p0, p1);
+      if constexpr (F8) {
+        if (i % 2 == 0) {
+          q0 = p0;
+          q1 = p1;
+        } else {
+          pk[i / 2] = to_e4m3x4(q0, q1, p0, p1);
+        }
+      } else {
+        pk[i] = pack2<false>(p0, p1);
+      }
     }
     sum2[0] = f2_add(f2_add(sum2[0], sum2[1]), f2_add(sum2[2], sum2[3]));
     float sum_lo, sum_hi;
@@ -572,9 +655,10 @@ __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const Softm
         tmem_st32(o_tmem + ch * 32, v);
       }
     }
-    // P (bf16) over the first 64 columns of this query tile's score columns.
+    // P over the first 64 (bf16) or 32 (e4m3) columns of this query tile's
+    // score columns.
 #pragma unroll
-    for (int ch = 0; ch < kKeys / 64; ++ch) {
+    for (int ch = 0; ch < kPk / 32; ++ch) {
       uint32_t v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = pk[ch * 32 + i];
@@ -633,14 +717,15 @@ __device__ __forceinline__ bool softmax_tile(const PrefillParams& p, const Softm
 }
 
 // Softmax warpgroup of query tile t over the CTA's work tiles.
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ void softmax_role(const PrefillParams& p, const uint8_t* ring, int t,
-                                             uint8_t* sV, uint32_t tmem, const Bars<D>& bar,
+                                             uint8_t* sQ, uint8_t* sV, uint32_t tmem,
+                                             const Bars<D, F8>& bar,
                                              volatile int32_t* abort, int warp, int lane) {
   int done = 0, step = 0;
   for (int k = 0;; ++k) {
     Item it;
-    if (!__all_sync(0xffffffffu, take_item<D>(p, bar, ring, k, it, abort))) {
+    if (!__all_sync(0xffffffffu, take_item<D, F8>(p, bar, ring, k, it, abort))) {
       give_up(p, abort);
       return;
     }
@@ -658,7 +743,7 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const uint8
     st.n_t = t ? it.g.ntiles[1] : it.g.ntiles[0];
     st.rows_t = t ? it.g.rows[1] : it.g.rows[0];
     if (st.n_t > 0) {
-      if (!softmax_tile<D>(p, st, t, done, step, sV, tmem, bar, abort, warp, lane)) {
+      if (!softmax_tile<D, F8>(p, st, t, done, step, sQ, sV, tmem, bar, abort, warp, lane)) {
         give_up(p, abort);
         return;
       }
@@ -668,12 +753,12 @@ __device__ __forceinline__ void softmax_role(const PrefillParams& p, const uint8
   }
 }
 
-template <int D>
+template <int D, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_q,
                    const __grid_constant__ CUtensorMap map_k,
                    const __grid_constant__ CUtensorMap map_v, const PrefillParams p) {
-  using L = Smem<D>;
+  using L = Smem<D, F8>;
   constexpr int KS = L::kKStages, VS = L::kVStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
@@ -681,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sQ = sm + L::kQ;
   uint8_t* sK = sm + L::kK;
   uint8_t* sV = sm + L::kV;
-  const Bars<D> bar{smem_u32(sm + L::kBar)};
+  const Bars<D, F8> bar{smem_u32(sm + L::kBar)};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kMisc);
   volatile int32_t* abort = reinterpret_cast<volatile int32_t*>(sm + L::kMisc + 8);
   volatile int32_t* never = reinterpret_cast<volatile int32_t*>(sm + L::kMisc + 12);
@@ -699,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort = 0;
     *never = 0;
     for (int t = 0; t < kTilesPerCta; ++t) {
-      mbar_init(bar.q_full(t), 1);
+      mbar_init(bar.q_full(t), F8 ? kRows : 1);  // F8: the softmax threads write Q
       mbar_init(bar.q_empty(t), 1);
     }
     for (int s = 0; s < KS; ++s) {
@@ -731,19 +816,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     if (warp == 0 && lane == 0) {
-      producer_role<D, false>(&map_q, &map_k, p, ring, sQ, sK, bar.kfull(0), bar.kempty(0), bar,
+      producer_role<D, F8, false>(&map_q, &map_k, p, ring, sQ, sK, bar.kfull(0), bar.kempty(0), bar,
                               abort, never);
     } else if (warp == 2 && lane == 0) {
-      producer_role<D, true>(&map_q, &map_v, p, ring, sQ, sV, bar.vfull(0), bar.vempty(0), bar,
+      producer_role<D, F8, true>(&map_q, &map_v, p, ring, sQ, sV, bar.vfull(0), bar.vempty(0), bar,
                              abort, never);
     } else if (warp == 1 && lane == 0) {
-      mma_role<D>(p, ring, sQ, sK, sV, tmem, bar, abort, never);
+      mma_role<D, F8>(p, ring, sQ, sK, sV, tmem, bar, abort, never);
     } else if (warp == 3 && lane == 0) {
-      scheduler_role<D>(p, bar, ring, abort);
+      scheduler_role<D, F8>(p, bar, ring, abort);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-    softmax_role<D>(p, ring, (warp - 4) / 4, sV, tmem, bar, abort, warp, lane);
+    softmax_role<D, F8>(p, ring, (warp - 4) / 4, sQ, sV, tmem, bar, abort, warp, lane);
   }
   tc_fence_before();
   __syncthreads();
@@ -754,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && p.span_end != nullptr) atomicMax(p.span_end, globaltimer_ns());
 }
 
-template <int D>
+template <int D, bool F8>
 cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                      const PrefillParams& p, cudaStream_t stream) {
   // The register split above assumes the launch budget; refuse to launch a
@@ -762,15 +847,15 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   static int checked = 0;
   if (!checked) {
     cudaFuncAttributes attr;
-    cudaError_t e = cudaFuncGetAttributes(&attr, prefill_kernel<D>);
+    cudaError_t e = cudaFuncGetAttributes(&attr, prefill_kernel<D, F8>);
     if (e != cudaSuccess) return e;
     if (attr.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
     checked = 1;
   }
   static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = set_smem_once(prefill_kernel<D>, Smem<D>::kAlloc, smem_set);
+  cudaError_t e = set_smem_once(prefill_kernel<D, F8>, Smem<D, F8>::kAlloc, smem_set);
   if (e != cudaSuccess) return e;
-  prefill_kernel<D><<<p.num_ctas, kThreads, Smem<D>::kAlloc, stream>>>(mq, mk, mv, p);
+  prefill_kernel<D, F8><<<p.num_ctas, kThreads, Smem<D, F8>::kAlloc, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -806,8 +891,31 @@ cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_
     e = encode_kv_page_map(&mv, v_cache, 2, head_dim, num_kv_heads, p.block_size, p.num_blocks,
                            64, p.rows_per_box, true);
   if (e != cudaSuccess) return e;
-  return head_dim == 128 ? launch_d<128>(mq, mk, mv, p, stream)
-                         : launch_d<64>(mq, mk, mv, p, stream);
+  return head_dim == 128 ? launch_d<128, false>(mq, mk, mv, p, stream)
+                         : launch_d<64, false>(mq, mk, mv, p, stream);
+}
+
+bool prefill_fp8_products_supported(int head_dim, int qpk, int block_size) {
+  return head_dim == 128 && qpk >= 1 && qpk <= kRows && kRows % qpk == 0 && block_size >= 16 &&
+         (kKeys % block_size == 0 || block_size % kKeys == 0);
+}
+
+cudaError_t launch_prefill_fp8_products(const PrefillParams& p, const void* k_cache,
+                                        const void* v_cache, int num_kv_heads,
+                                        cudaStream_t stream) {
+  if (p.num_tiles <= 0 || p.num_ctas <= 0) return cudaSuccess;
+  if (p.counters == nullptr || p.q == nullptr) return cudaErrorInvalidValue;
+  // K/V pages of e4m3 codes: (128 dims = one 128-byte panel, one head,
+  // rows_per_box slots, one block) per box. Q is read by the softmax warps;
+  // its tensor map argument is not used (the K map stands in for it).
+  CUtensorMap mk, mv;
+  cudaError_t e = encode_kv_page_map(&mk, k_cache, 1, 128, num_kv_heads, p.block_size,
+                                     p.num_blocks, 128, p.rows_per_box, true);
+  if (e == cudaSuccess)
+    e = encode_kv_page_map(&mv, v_cache, 1, 128, num_kv_heads, p.block_size, p.num_blocks, 128,
+                           p.rows_per_box, true);
+  if (e != cudaSuccess) return e;
+  return launch_d<128, true>(mk, mk, mv, p, stream);
 }
 
 }  // namespace ua

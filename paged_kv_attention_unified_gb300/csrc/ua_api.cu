@@ -42,6 +42,7 @@ struct ua_plan {
   float unified_max = 0.f;
   uint64_t wait_timeout_ns = 2000000000ull;
   int32_t prefill_ctas_override = 0;  // ua_plan_set_prefill_ctas (0: the scheduler's count)
+  bool fp8_products = false;          // ua_plan_set_fp8_products
   // kernel timing (ua_plan_set_profiling)
   struct EventPair {
     cudaEvent_t start = nullptr, stop = nullptr;
@@ -532,7 +533,10 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
                                     block_tables, num_blocks, scale, k_scale, v_scale);
   const bool mixed = !s.prefill.empty() && !s.decode.empty();
   auto run_prefill = [&](cudaStream_t cs) -> ua_status {
-    const bool staged = plan->prob.prefill_staged;
+    // fp8 cache: either the prefill kernel reads a bf16 staging copy, or (fp8
+    // products on) the fp8-products kernel reads the e4m3 cache itself
+    const bool f8p = plan->prob.prefill_staged && plan->fp8_products;
+    const bool staged = plan->prob.prefill_staged && !f8p;
     const void* pk = k_cache;
     const void* pv = v_cache;
     if (staged) {
@@ -561,6 +565,7 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     std::memset(&pp, 0, sizeof(pp));
     pp.tiles = plan->d_prefill;
     pp.num_tiles = static_cast<int32_t>(s.prefill.size());
+    pp.q = q;
     pp.counters = plan->d_prefill_counters;
     pp.num_ctas = plan->prefill_ctas_override > 0
                       ? std::min<int32_t>(plan->prefill_ctas_override,
@@ -593,10 +598,11 @@ ua_status ua_forward(const ua_plan* plan, const void* q, const void* k_cache,
     if (mixed) span_begin(mp, 0, &pp.span_start, &pp.span_end);
     else ev = timing_begin(mp, 0, cs);
     const cudaError_t le =
-        wide ? ua::launch_prefill_wide(pp, q, pk, pv, plan->total_q, plan->prob.head_dim,
-                                       plan->prob.num_kv_heads, cs)
-             : ua::launch_prefill(pp, q, pk, pv, plan->total_q, plan->prob.head_dim,
-                                  plan->prob.num_kv_heads, cs);
+        f8p  ? ua::launch_prefill_fp8_products(pp, k_cache, v_cache, plan->prob.num_kv_heads, cs)
+        : wide ? ua::launch_prefill_wide(pp, q, pk, pv, plan->total_q, plan->prob.head_dim,
+                                         plan->prob.num_kv_heads, cs)
+               : ua::launch_prefill(pp, q, pk, pv, plan->total_q, plan->prob.head_dim,
+                                    plan->prob.num_kv_heads, cs);
     if (le != cudaSuccess) return UA_ERR_CUDA;
     timing_end(ev, cs);
     return UA_OK;
@@ -878,6 +884,19 @@ ua_status ua_plan_set_debug(ua_plan* plan, int32_t flags, int64_t wait_timeout_n
 ua_status ua_plan_set_prefill_ctas(ua_plan* plan, int32_t num_ctas) {
   if (plan == nullptr || num_ctas < 0) return UA_ERR_INVALID_ARG;
   plan->prefill_ctas_override = num_ctas;
+  return UA_OK;
+}
+
+ua_status ua_plan_set_fp8_products(ua_plan* plan, int32_t enable) {
+  if (plan == nullptr || (enable != 0 && enable != 1)) return UA_ERR_INVALID_ARG;
+  if (enable) {
+    const ua::Problem& pr = plan->prob;
+    if (pr.kv_dtype != UA_KV_FP8_E4M3 || !pr.prefill_staged ||
+        !ua::prefill_fp8_products_supported(pr.head_dim, pr.num_q_heads / pr.num_kv_heads,
+                                            pr.block_size))
+      return UA_ERR_UNSUPPORTED;
+  }
+  plan->fp8_products = enable != 0;
   return UA_OK;
 }
 

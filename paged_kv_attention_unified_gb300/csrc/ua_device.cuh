@@ -127,6 +127,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
+// Four binary32 values -> four e4m3 codes (x0 in the lowest byte), rounded
+// to nearest even and saturating.
+__device__ __forceinline__ uint32_t to_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint16_t lo, hi;
+  // the first source operand lands in the upper byte of the pair
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// The two bf16 values of a 32-bit word as binary32 (exact).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
 // Two e4m3 codes in the low 16 bits -> f16x2 (low byte -> low half). Exact:
 // every e4m3 value is an f16 value.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {

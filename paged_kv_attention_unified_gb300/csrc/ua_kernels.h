@@ -29,6 +29,7 @@ cudaError_t set_smem_once(Kernel kernel, int bytes, std::atomic<uint64_t>& done)
 struct PrefillParams {
   const ua_tile* tiles;       // taken in list order by the persistent CTAs
   int32_t num_tiles;
+  const void* q;              // bf16 queries (read directly by the fp8-products kernel)
   int32_t* counters;          // [2] next tile, finished CTAs; zero between launches
   int32_t num_ctas;           // persistent CTAs (at most one per SM)
   const int32_t* cu_query_lens;
@@ -69,6 +70,16 @@ bool prefill_supported(int head_dim, int kv_dtype, int qpk, int block_size);
 cudaError_t launch_prefill(const PrefillParams& p, const void* q, const void* k_cache,
                            const void* v_cache, int64_t total_q, int head_dim,
                            int num_kv_heads, cudaStream_t stream);
+
+// Prefill kernel with fp8 tensor-core products over an e4m3 cache (head_dim
+// 128): Q rows quantised to e4m3 per row inside the kernel, S = Q K^T and
+// O += P V as kind::f8f6f4 MMAs with P rounded to e4m3. rows_per_box as for
+// launch_prefill; score_scale_log2 = scale * log2(e) * k_scale, out_scale =
+// v_scale.
+bool prefill_fp8_products_supported(int head_dim, int qpk, int block_size);
+cudaError_t launch_prefill_fp8_products(const PrefillParams& p, const void* k_cache,
+                                        const void* v_cache, int num_kv_heads,
+                                        cudaStream_t stream);
 
 // head_dim 192 / 256 prefill kernel (one 128-row query tile at a time,
 // 64-key tiles): whether it takes the problem, the keys per TMA box it needs

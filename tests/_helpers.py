@@ -55,3 +55,13 @@ def assert_close(got: np.ndarray, exp: np.ndarray, kv_dtype: str, what: str = ""
         assert mx <= BF16_MAX_ABS, f"{what}: max-abs {mx:.3e} > {BF16_MAX_ABS}"
         assert mean <= BF16_MEAN_ABS, f"{what}: mean-abs {mean:.3e} > {BF16_MEAN_ABS}"
     return mx, mean
+
+
+def oracle_fp8_products(case):
+    """The fp8-products oracle (e4m3 Q rows, e4m3 P) of an fp8-cache case."""
+    from oracle import fp8_products as F
+    r = case.raw()
+    return F.paged_attention_fp8_products(r["q"], r["k_cache"], r["v_cache"], r["cu_query_lens"],
+                                          r["kv_lens"], r["block_tables"], case.block_size,
+                                          case.scale, k_scale=case.k_scale, v_scale=case.v_scale,
+                                          causal=case.causal, window=case.window)

@@ -375,3 +375,8 @@ def test_head_dim_256_prefills_go_to_the_wide_prefill_kernel():
     assert len(rows) == (1 + 300) * 4 * 2
     info, pre, dec, _ = ua.ua_schedule([0, 1, 301], [500, 800], 8, 2, 256, 48, 17)
     assert info.num_prefill_tiles == 0 and info.num_decode_tiles > 0
+
+def test_fp8_products_setter_rejects_a_null_plan_without_touching_cuda():
+    lib = ua.lib()
+    assert lib.ua_plan_set_fp8_products(None, 1) == ua.UA_ERR_INVALID_ARG
+    assert lib.ua_plan_set_fp8_products(None, 0) == ua.UA_ERR_INVALID_ARG

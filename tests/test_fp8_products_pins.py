@@ -125,11 +125,13 @@ def test_two_keys_closed_form():
     assert np.allclose(out[0, 0], expect, rtol=1e-14, atol=1e-14)
 
 
-def _grid_problem(seed, kv_list, hq, hkv, d=16, late_max=True):
-    """Every quantisation step exact: q rows 448 e_0 (inv = 1), key values k in
-    {0, 1/8, ..., 1} at dimension 0 and scale with 448 * scale = 8 ln 2, so
-    every score difference is a multiple of ln 2 and every p relative to any
-    running max is 2^-j, 0 <= j <= 8 (all e4m3 values)."""
+def _grid_problem(seed, kv_list, hq, hkv, d=16):
+    """Every quantisation step exact: q rows 448 e_0 (inv = 1), key values at
+    dimension 0 on a grid of 1/8 and scale with 448 * scale = 8 ln 2, so every
+    score is a multiple of ln 2 (8 k in log2 units). Keys 0..127 score 0..3,
+    later keys 4..12, and the key at 130 scores 12: the reference moves once,
+    at the second block (12 > 3 + 8), and every p relative to it is 2^-j with
+    0 <= j <= 8 (all e4m3 values)."""
     rng = np.random.default_rng(seed)
     tq = len(kv_list)
     q = np.zeros((tq, hq, d), dtype=np.float32)
@@ -137,9 +139,12 @@ def _grid_problem(seed, kv_list, hq, hkv, d=16, late_max=True):
     kvals, vvals = [], []
     for n in kv_list:
         k = np.zeros((n, hkv, d))
-        k[:, :, 0] = rng.integers(0, 8, size=(n, hkv)) / 8.0
-        if late_max:
-            k[n - 1, :, 0] = 1.0        # the largest score sits in the last block
+        first = min(n, 128)
+        k[:first, :, 0] = rng.integers(0, 4, size=(first, hkv)) / 8.0
+        if n > 128:
+            k[128:, :, 0] = rng.integers(4, 13, size=(n - 128, hkv)) / 8.0
+        if n > 130:
+            k[130, :, 0] = 12.0 / 8.0
         k[:, :, 1:] = _vals(rng, (n, hkv, d - 1), 120)
         kvals.append(k)
         vvals.append(_vals(rng, (n, hkv, d)))
@@ -151,13 +156,34 @@ def _grid_problem(seed, kv_list, hq, hkv, d=16, late_max=True):
 def test_exact_grid_equals_the_unquantised_oracle(causal, window):
     """On the exact grid the fp8-products path computes the plain softmax:
     it must equal the exact oracle (oracle.paged_attention) to rounding, over
-    many blocks whose running max moves late (alpha != 1)."""
+    many blocks, with a reference that moves (alpha != 1)."""
     (q, kc, vc, cu, kv, bt), scale = _grid_problem(14, [700, 129, 1, 300], 4, 2)
     got = F.paged_attention_fp8_products(q, kc, vc, cu, kv, bt, 16, scale, k_scale=1.0,
                                          v_scale=0.75, causal=causal, window=window)
     exp, _ = oracle.paged_attention(q, kc, vc, cu, kv, bt, 16, scale, kv_dtype="fp8_e4m3",
                                     k_scale=1.0, v_scale=0.75, causal=causal, window=window)
     assert np.allclose(got, exp, rtol=0, atol=1e-12)
+
+
+def test_lagging_reference_keeps_p_up_to_256():
+    """Scores 0 and 8 ln 2 in two blocks: the second block's max exceeds the
+    reference by exactly 2^8, which does not move it, so that key's p is 256
+    (an e4m3 value) and the output is (v0 + 256 v1) / 257."""
+    d = 4
+    q = np.zeros((1, 1, d), dtype=np.float32)
+    q[0, 0, 0] = 448.0
+    n = 129
+    k = np.zeros((n, 1, d))
+    k[128, 0, 0] = 1.0
+    v = np.zeros((n, 1, d))
+    v[0, 0] = [1.0, 2.0, -4.0, 0.5]
+    v[128, 0] = [8.0, -1.0, 0.25, 3.0]
+    # keys 1..127 score like key 0 but carry zero values
+    raw = _problem(q, [k], [v], [0, 1], [n], 1, 1)
+    out = F.paged_attention_fp8_products(*raw, block_size=16, scale=8 * math.log(2) / 448.0,
+                                         causal=False)
+    expect = (v[0, 0] * 0 + 256.0 * v[128, 0]) / (128 + 256.0)
+    assert np.allclose(out[0, 0], expect + v[0, 0] / 384.0, rtol=1e-13, atol=1e-13)
 
 
 def test_mutation_unrounded_p_is_caught(monkeypatch):
@@ -181,7 +207,9 @@ def test_mutation_stale_alpha_is_caught(monkeypatch):
             cols = (keys >= b0) & (keys < b0 + block_n)
             mask = vis[:, cols]
             sb = np.where(mask, S[:, cols], -np.inf)
-            m = np.maximum(m, np.max(sb, axis=1))
+            bm = np.max(sb, axis=1)
+            with np.errstate(invalid="ignore"):
+                m = np.where(~np.isfinite(m) | (bm > m + F.LAG), np.maximum(m, bm), m)
             p = np.where(mask, real_exp(sb - np.where(np.isfinite(m), m, 0)[:, None]), 0.0)
             l = l + p.sum(axis=1)
             acc = acc + F.round_e4m3(p) @ V8[cols]
