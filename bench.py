@@ -47,8 +47,13 @@ WORKLOAD_NAMES = {
        "(not a benchmark configuration: measures the head_dim 256 decode path)",
     9: "dense causal prefill at head_dim 256: 4 seqs x 4096, 32/32 heads, bf16, bs128, identity "
        "table (not a benchmark configuration: measures the head_dim 256 prefill kernel)",
+    10: "pure decode at head_dim 96: 64 seqs, q 1, kv U[512,4096], 32/8 heads, bf16, bs16 "
+        "(not a benchmark configuration: measures the decode kernel at a non-power-of-two "
+        "head dim)",
+    11: "dense causal prefill at head_dim 192: 4 seqs x 4096, 32/32 heads, bf16, bs128, "
+        "identity table (not a benchmark configuration: measures the head_dim 192 prefill)",
 }
-FLOP_CONFIGS = (4, 6, 9)   # prefill-bound workloads, reported in TFLOP/s
+FLOP_CONFIGS = (4, 6, 9, 11)   # prefill-bound workloads, reported in TFLOP/s
 
 
 def _seq_work(case):

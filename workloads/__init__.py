@@ -298,6 +298,26 @@ def config9_dense_prefill_d256(seed: int = 0, poison: bool = False) -> Case:
                      256, 128, table="identity", seed=seed, poison=poison)
 
 
+def config10_pure_decode_d96(seed: int = 0, poison: bool = False) -> Case:
+    """Config 2's batch at head_dim 96 (rows of 192 bytes: not whole 128-byte
+    panels): 64 decode sequences, kv_len ~ U[512, 4096], 32 q / 8 kv heads,
+    bf16 (not one of the five benchmark configurations: it measures the
+    decode kernel at a head dim that is not a power of two)."""
+    gen = torch.Generator().manual_seed(seed)
+    kv = torch.randint(512, 4097, (64,), generator=gen).tolist()
+    return make_case("pure_decode_b64_kv512-4096_h32-8_d96_bf16", [1] * 64, kv, 32, 8, 96, 16,
+                     gen=gen, poison=poison)
+
+
+def config11_dense_prefill_d192(seed: int = 0, poison: bool = False) -> Case:
+    """Config 4's dense causal prefill at head_dim 192: batch 4, 32 heads
+    (MHA), q = kv = 4096, bf16, block_size 128, identity table (not one of the
+    five benchmark configurations: it measures the wide prefill kernel at
+    head_dim 192)."""
+    return make_case("dense_causal_prefill_b4_h32_l4096_d192", [4096] * 4, [4096] * 4, 32, 32,
+                     192, 128, table="identity", seed=seed, poison=poison)
+
+
 CONFIGS = {
     1: config1_tiny_mixed,
     2: config2_pure_decode,
@@ -308,6 +328,8 @@ CONFIGS = {
     7: config7_uniform_decode,
     8: config8_pure_decode_d256,
     9: config9_dense_prefill_d256,
+    10: config10_pure_decode_d96,
+    11: config11_dense_prefill_d192,
 }
 
 
