@@ -307,7 +307,7 @@ def run_reference(args):
     return 0
 
 
-def _traffic_record(kernel: str, cfg: int):
+def _traffic_record(kernel: str, cfg):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current sources (profiles/traffic.json: {key: {"source_hash", "bytes"}}).
     Returns (bytes or None, note, {"current": digest, "record": digest})."""
@@ -468,7 +468,8 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
                        "kernels of a mixed step overlap), over K steps after the timed ones") \
             if mixed else "CUDA events on the launching stream, over K steps after the timed ones"
         traffic, note, digests = _traffic_record(
-            "prefill_wide" if kind == "prefill" and case.head_dim == 256 else kind, cfg)
+            "prefill_wide" if kind == "prefill" and case.head_dim in (192, 256) else kind,
+            f"{cfg}f8p" if f8p and kind == "prefill" else cfg)
         r["traffic"] = traffic
         if note:
             r["traffic_note"] = note
