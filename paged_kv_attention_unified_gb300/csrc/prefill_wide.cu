@@ -185,6 +185,25 @@ __device__ __forceinline__ void load_key_tile(const CUtensorMap* map, const Pref
   const int boxes = kKeys / p.rows_per_box;
   const int base = it.kv_lo + j * kKeys;
   mbar_arrive_expect_tx(full, kStage);
+  if (boxes == 1) {
+    // Pages of at least a key tile: one box (and one page-table load).
+    int32_t blk = static_cast<int32_t>(p.num_blocks);  // out of range: zero fill
+    int32_t slot = 0;
+    if (base < it.kv_hi) {
+      const int32_t id =
+          p.block_tables[static_cast<int64_t>(it.seq) * p.max_blocks_per_seq + base / p.block_size];
+      if (id >= 0 && static_cast<int64_t>(id) < p.num_blocks) {
+        blk = id;
+        slot = base % p.block_size;
+      } else {
+        record_error(p.err, UA_ERR_BOUNDS);
+      }
+    }
+#pragma unroll
+    for (int pn = 0; pn < kPanels; ++pn)
+      tma_load_4d(dst + pn * kPanelKV, map, full, pn * 64, it.kv_head, slot, blk);
+    return;
+  }
   for (int b = 0; b < boxes; ++b) {
     const int key0 = base + b * p.rows_per_box;
     int32_t blk = static_cast<int32_t>(p.num_blocks);  // out of range: zero fill
