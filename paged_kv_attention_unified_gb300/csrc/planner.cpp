@@ -193,8 +193,14 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
     const int64_t slots = static_cast<int64_t>(num_sms) * decode_ctas_per_sm(p.head_dim, p.kv_dtype == UA_KV_BF16 ? 2 : 1);
     chunk = round_up(std::max<int64_t>(kMinSplitTokens, ceil_div(total, slots)), kKeyStep);
     chunk = std::max<int64_t>(chunk, round_up(ceil_div(longest, UA_MAX_SPLITS), kKeyStep));
-    if (chunk < longest && shortest * 16 >= longest * 15)
-      chunk = wave_fit_chunk(static_cast<int64_t>(dec.size()), longest, slots);
+    if (chunk < longest && shortest * 16 >= longest * 15) {
+      // Tiles of (nearly) one length: unsplit when they alone fill HBM in
+      // one wave (bf16, rows of at least 256 bytes), else whole waves.
+      const int64_t t = static_cast<int64_t>(dec.size());
+      const bool saturating = p.kv_dtype == UA_KV_BF16 && p.head_dim >= 128 &&
+                              t >= kDecodeSaturatingCtas && t <= slots;
+      chunk = saturating ? longest : wave_fit_chunk(t, longest, slots);
+    }
     if (chunk >= longest) chunk = 0;
   }
   s.split_tokens = static_cast<int32_t>(chunk);

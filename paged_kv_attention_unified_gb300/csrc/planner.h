@@ -110,6 +110,13 @@ static_assert(decode_ctas_per_sm(128) == 3 && decode_ctas_per_sm(256) == 1 &&
 // Cost of one split piece beyond its keys (CTA start, ring fill, merge and
 // store), in key tokens: used when automatic splits are fitted to whole waves.
 constexpr int kPieceOverheadTokens = 128;
+// bf16 decode CTAs (head_dim >= 128) that keep HBM busy by themselves: each
+// keeps 64 KB or more of K/V in flight, and 256 unsplit tiles of 8192 keys
+// (one per CTA, 1.7 per SM) stream at 0.99 of the copy peak, while cutting
+// them into waves of 456 pieces loses 10 % to the extra pieces and the wave
+// tails. Uniform batches with at least this many tiles in one wave stay
+// unsplit.
+constexpr int kDecodeSaturatingCtas = 256;
 // Smallest automatic split piece, in key tokens.
 constexpr int kMinSplitTokens = 256;
 // Default: sequences with q_len * qpk above this go to the prefill kernel

@@ -319,14 +319,29 @@ def test_uniform_decode_splits_fill_whole_waves():
     lens = _piece_lengths(dec)
     assert max(lens) - min(lens) <= 16 * 7
     assert all(g["nsplits"] == 7 for g in grp)
-    # 256 tiles of 8192 keys: the chosen cut beats both the average-load chunk
-    # (2 pieces, 512 CTAs: 2 waves of 4608 keys) and no split (8192 keys)
-    info, _, dec, _ = _check_schedule(list(range(33)), [8192] * 32, 32, 8)
+    # 128 tiles of 16384 keys (too few to fill HBM unsplit): the chosen cut
+    # beats both the average-load chunk (4608 keys: 4 pieces, 512 CTAs, 2
+    # waves) and no split (16384 keys)
+    info, _, dec, grp = _check_schedule(list(range(17)), [16384] * 16, 32, 8)
     lens = _piece_lengths(dec)
-    per_tile = len(dec) // 256
-    assert _waves(len(dec), 456) * (max(lens) + 128) < min(2 * (4608 + 128), 8192 + 128)
-    assert all(g["nsplits"] == per_tile for g in _check_schedule(
-        list(range(33)), [8192] * 32, 32, 8)[3])
+    per_tile = len(dec) // 128
+    assert per_tile > 1
+    assert _waves(len(dec), 456) * (max(lens) + 128) < min(2 * (4608 + 128), 16384 + 128)
+    assert all(g["nsplits"] == per_tile for g in grp)
+
+
+def test_uniform_bf16_batches_that_fill_hbm_stay_unsplit():
+    """256 tiles of 8192 keys (bf16, d128): one CTA each, 1.7 per SM, already
+    stream at the copy peak, so they stay unsplit; the same batch over an
+    e4m3 cache (whose CTAs are slower) and a 255-tile batch are split."""
+    info, _, dec, _ = _check_schedule(list(range(33)), [8192] * 32, 32, 8)
+    assert len(dec) == 256 and info.num_combine_groups == 0 and info.split_tokens == 0
+    info, _, dec, _ = ua.ua_schedule(list(range(33)), [8192] * 32, 32, 8, 128, 16, 513,
+                                     kv_dtype=ua.UA_KV_FP8_E4M3)
+    assert len(dec) > 256
+    # 255 tiles: fewer than the saturating count, so split into whole waves
+    info, _, dec, _ = ua.ua_schedule(list(range(256)), [8192] * 255, 8, 1, 128, 16, 513)
+    assert len(dec) > 255
 
 
 def test_nonuniform_decode_keeps_the_average_load_chunk():
