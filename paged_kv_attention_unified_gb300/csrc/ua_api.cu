@@ -398,7 +398,10 @@ ua_status create_plan(ua_plan** out, const int32_t* cu_query_lens_host,
     return UA_ERR_CUDA;
   }
   uint8_t* host = static_cast<uint8_t*>(staging.ptr);
-  std::memset(host, 0, bytes_meta);
+  // Every list below is copied whole; only the error word, the combine
+  // counters and the prefill queue counters (and the padding up to the
+  // append tiles) start at zero.
+  std::memset(host + bytes_tiles + bytes_groups, 0, off_app - (bytes_tiles + bytes_groups));
   if (n_pre) std::memcpy(host, s.prefill.data(), n_pre * sizeof(ua_tile));
   if (n_dec) std::memcpy(host + n_pre * sizeof(ua_tile), s.decode.data(),
                          n_dec * sizeof(ua_tile));
