@@ -3,6 +3,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <functional>
 
 namespace ua {
 
@@ -51,6 +52,11 @@ int64_t wave_fit_chunk(int64_t tiles, int64_t len, int64_t slots) {
     }
   }
   return best_size;
+}
+
+// Work of a tile: keys read x packed rows.
+inline int64_t work_of(const ua_tile& t) {
+  return static_cast<int64_t>(t.kv_hi - t.kv_lo) * t.nrows;
 }
 
 // Indices 0..n-1 ordered by the keys (a, b, c) ascending, ties by index: a
@@ -120,18 +126,30 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
                            : (p.decode_rows_max < 0 ? kDefaultDecodeRowsMax : p.decode_rows_max);
   const int num_sms = p.num_sms > 0 ? p.num_sms : 152;
 
-  // 1. Whole decode tiles (before splitting) and prefill tiles.
-  std::vector<ua_tile> dec;
+  // 1. Prefill tiles, and the decode row blocks: a decode sequence's packed
+  // rows in runs of UA_DECODE_ROWS with their key ranges, which are the same
+  // for each of its KV heads (its tiles are (KV head, row block) in that
+  // order).
+  struct DecodeBlock {
+    int32_t seq, row0, nrows, kv_lo, kv_hi;
+  };
+  std::vector<DecodeBlock> blocks;
+  std::vector<int32_t> span_end;  // per decode sequence: end of its blocks
   {
-    int64_t n_dec = 0, n_pre = 0, n_app = 0;
+    int64_t n_blk = 0, n_pre = 0, n_app = 0, n_dseq = 0;
     for (int32_t q = 0; q < p.num_seqs; ++q) {
       const int64_t ql = p.cu_query_lens[q + 1] - p.cu_query_lens[q];
       const int64_t rows = ql * qpk;
-      if (rows <= rows_max) n_dec += ceil_div(rows, UA_DECODE_ROWS) * p.num_kv_heads;
-      else n_pre += ceil_div(rows, UA_PREFILL_ROWS) * p.num_kv_heads;
+      if (rows <= rows_max) {
+        n_blk += ceil_div(rows, UA_DECODE_ROWS);
+        ++n_dseq;
+      } else {
+        n_pre += ceil_div(rows, UA_PREFILL_ROWS) * p.num_kv_heads;
+      }
       n_app += ceil_div(ql, kAppendTokens);
     }
-    dec.reserve(static_cast<size_t>(n_dec));
+    blocks.reserve(static_cast<size_t>(n_blk));
+    span_end.reserve(static_cast<size_t>(n_dseq));
     s.prefill.reserve(static_cast<size_t>(n_pre));
     s.append.reserve(static_cast<size_t>(n_app));
   }
@@ -143,20 +161,37 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
     if (ql == 0) continue;
     const int32_t ctx = kv - ql;
     const int64_t rows = static_cast<int64_t>(ql) * qpk;
-    const bool is_decode = rows <= rows_max;
-    const int step = is_decode ? UA_DECODE_ROWS : UA_PREFILL_ROWS;
-    for (int32_t g = 0; g < p.num_kv_heads; ++g) {
-      for (int64_t r0 = 0; r0 < rows; r0 += step) {
-        ua_tile t;
-        t.seq = q;
+    if (rows <= rows_max) {
+      for (int64_t r0 = 0; r0 < rows; r0 += UA_DECODE_ROWS) {
+        DecodeBlock b;
+        b.seq = q;
+        b.row0 = static_cast<int32_t>(r0);
+        b.nrows = static_cast<int32_t>(std::min<int64_t>(UA_DECODE_ROWS, rows - r0));
+        key_range(p, ctx, kv, b.row0, b.nrows, &b.kv_lo, &b.kv_hi);
+        blocks.push_back(b);
+      }
+      span_end.push_back(static_cast<int32_t>(blocks.size()));
+      continue;
+    }
+    const size_t first = s.prefill.size();
+    for (int64_t r0 = 0; r0 < rows; r0 += UA_PREFILL_ROWS) {
+      ua_tile t;
+      t.seq = q;
+      t.kv_head = 0;
+      t.row0 = static_cast<int32_t>(r0);
+      t.nrows = static_cast<int32_t>(std::min<int64_t>(UA_PREFILL_ROWS, rows - r0));
+      key_range(p, ctx, kv, t.row0, t.nrows, &t.kv_lo, &t.kv_hi);
+      t.kv_lo = static_cast<int32_t>(round_down(t.kv_lo, kPrefillKeyTile));
+      t.slot = -1;
+      t.group = -1;
+      s.prefill.push_back(t);
+    }
+    const size_t per_head = s.prefill.size() - first;
+    for (int32_t g = 1; g < p.num_kv_heads; ++g) {
+      for (size_t i = 0; i < per_head; ++i) {
+        ua_tile t = s.prefill[first + i];
         t.kv_head = g;
-        t.row0 = static_cast<int32_t>(r0);
-        t.nrows = static_cast<int32_t>(std::min<int64_t>(step, rows - r0));
-        key_range(p, ctx, kv, t.row0, t.nrows, &t.kv_lo, &t.kv_hi);
-        if (!is_decode) t.kv_lo = static_cast<int32_t>(round_down(t.kv_lo, kPrefillKeyTile));
-        t.slot = -1;
-        t.group = -1;
-        (is_decode ? dec : s.prefill).push_back(t);
+        s.prefill.push_back(t);
       }
     }
   }
@@ -182,97 +217,206 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
 
   // 2. Split-KV for decode tiles (FlashDecoding): one chunk length C for the
   // whole batch, so that pieces are equal-sized and load-balance well.
+  const int64_t heads = p.num_kv_heads;
+  const int64_t n_tiles = static_cast<int64_t>(blocks.size()) * heads;
   int64_t total = 0, longest = 0, shortest = INT64_MAX;
-  for (const ua_tile& t : dec) {
-    total += t.kv_hi - t.kv_lo;
-    longest = std::max<int64_t>(longest, t.kv_hi - t.kv_lo);
-    shortest = std::min<int64_t>(shortest, t.kv_hi - t.kv_lo);
+  for (const DecodeBlock& b : blocks) {
+    total += (b.kv_hi - b.kv_lo) * heads;
+    longest = std::max<int64_t>(longest, b.kv_hi - b.kv_lo);
+    shortest = std::min<int64_t>(shortest, b.kv_hi - b.kv_lo);
   }
   int64_t chunk = 0;  // 0: do not split
-  if (p.num_splits == 0 && !dec.empty() && total > 0) {
-    const int64_t slots = static_cast<int64_t>(num_sms) * decode_ctas_per_sm(p.head_dim, p.kv_dtype == UA_KV_BF16 ? 2 : 1);
+  const int64_t slots = static_cast<int64_t>(num_sms) * decode_ctas_per_sm(p.head_dim, p.kv_dtype == UA_KV_BF16 ? 2 : 1);
+  if (p.num_splits == 0 && n_tiles > 0 && total > 0) {
     chunk = round_up(std::max<int64_t>(kMinSplitTokens, ceil_div(total, slots)), kKeyStep);
     chunk = std::max<int64_t>(chunk, round_up(ceil_div(longest, UA_MAX_SPLITS), kKeyStep));
     if (chunk < longest && shortest * 16 >= longest * 15) {
       // Tiles of (nearly) one length: unsplit when they alone fill HBM in
       // one wave (bf16, rows of at least 256 bytes), else whole waves.
-      const int64_t t = static_cast<int64_t>(dec.size());
       const bool saturating = p.kv_dtype == UA_KV_BF16 && p.head_dim >= 128 &&
-                              t >= kDecodeSaturatingCtas && t <= slots;
-      chunk = saturating ? longest : wave_fit_chunk(t, longest, slots);
+                              n_tiles >= kDecodeSaturatingCtas && n_tiles <= slots;
+      chunk = saturating ? longest : wave_fit_chunk(n_tiles, longest, slots);
     }
     if (chunk >= longest) chunk = 0;
   }
   s.split_tokens = static_cast<int32_t>(chunk);
-  s.decode.reserve(dec.size() + (chunk > 0 ? static_cast<size_t>(ceil_div(total, chunk)) : 0) +
-                   (p.num_splits > 0 ? dec.size() * static_cast<size_t>(p.num_splits) : 0));
-  int64_t slot = 0;
-  for (const ua_tile& t : dec) {
-    const int64_t len = t.kv_hi - t.kv_lo;
-    int64_t pieces = 1, size = len;
-    if (p.num_splits > 0) {
-      pieces = std::max<int64_t>(1, std::min<int64_t>(p.num_splits, ceil_div(len, kKeyStep)));
-      size = round_up(ceil_div(len, pieces), kKeyStep);
-      pieces = std::max<int64_t>(1, ceil_div(len, size));
-    } else if (chunk > 0 && len > chunk) {
-      size = chunk;
-      pieces = ceil_div(len, chunk);
+  // Tail pieces. Unsplit tiles that overfill one wave of CTA slots by at most
+  // half a wave leave a second wave of `late` whole tiles behind the first:
+  // the step takes two tile times for little more than one tile time of work.
+  // The `late` tiles that start last in the longest-first order below are cut
+  // into k = slots / late pieces (each of at least kMinSplitTokens keys), so
+  // they fill the slots the first wave frees and end a fraction of a tile
+  // after it.
+  int64_t tail_k = 0;
+  if (p.num_splits == 0 && chunk == 0 && n_tiles > slots) {
+    const int64_t k = std::min<int64_t>(UA_MAX_SPLITS, slots / (n_tiles - slots));
+    if (k >= 2) tail_k = k;
+  }
+
+  // Per block: the pieces of its tiles (size, count) in the batch rule and,
+  // with tail pieces, for a late tile.
+  struct Cut {
+    int64_t size, pieces;
+  };
+  auto cut = [](int64_t len, int64_t pieces) {
+    const int64_t size = round_up(ceil_div(len, pieces), kKeyStep);
+    return Cut{size, std::max<int64_t>(1, ceil_div(len, size))};
+  };
+  const size_t nb = blocks.size();
+  std::vector<Cut> plan(nb), late_plan(tail_k > 0 ? nb : 0);
+  for (size_t i = 0; i < nb; ++i) {
+    const int64_t len = blocks[i].kv_hi - blocks[i].kv_lo;
+    if (p.num_splits > 0)
+      plan[i] = cut(len, std::max<int64_t>(1, std::min<int64_t>(p.num_splits, ceil_div(len, kKeyStep))));
+    else if (chunk > 0 && len > chunk)
+      plan[i] = Cut{chunk, ceil_div(len, chunk)};
+    else
+      plan[i] = Cut{len, 1};
+    if (tail_k > 0) {
+      const int64_t n = std::min<int64_t>(tail_k, len / kMinSplitTokens);
+      late_plan[i] = n >= 2 ? cut(len, n) : Cut{len, 1};
     }
-    if (pieces <= 1) {
-      s.decode.push_back(t);
-      continue;
+  }
+
+  // 3. Longest work (keys x rows) first, so the tail of the grid holds the
+  // short pieces; equal work in (sequence, KV head, row, key) order, the
+  // generation order. The distinct works are few (at most four per block:
+  // whole and last piece, in each plan): pieces are counted per work, then
+  // written in generation order straight to their place.
+  // work of a full piece and of the last piece of a tile of block b cut by c
+  auto whole_work = [](const DecodeBlock& b, const Cut& c) { return c.size * b.nrows; };
+  auto last_work = [](const DecodeBlock& b, const Cut& c) {
+    return (b.kv_hi - b.kv_lo - (c.pieces - 1) * c.size) * b.nrows;
+  };
+  std::vector<int64_t> works;
+  works.reserve(4 * nb);
+  for (size_t i = 0; i < nb; ++i) {
+    works.push_back(whole_work(blocks[i], plan[i]));
+    works.push_back(last_work(blocks[i], plan[i]));
+    if (tail_k > 0) {
+      works.push_back(whole_work(blocks[i], late_plan[i]));
+      works.push_back(last_work(blocks[i], late_plan[i]));
     }
-    ua_combine_group grp;
-    grp.seq = t.seq;
-    grp.kv_head = t.kv_head;
-    grp.row0 = t.row0;
-    grp.nrows = t.nrows;
-    grp.slot0 = static_cast<int32_t>(slot);
-    grp.nsplits = static_cast<int32_t>(pieces);
-    grp.pad0 = grp.pad1 = 0;
-    const int32_t gid = static_cast<int32_t>(s.groups.size());
-    s.groups.push_back(grp);
-    for (int64_t k = 0; k < pieces; ++k) {
-      ua_tile piece = t;
-      piece.kv_lo = static_cast<int32_t>(t.kv_lo + k * size);
-      piece.kv_hi = static_cast<int32_t>(std::min<int64_t>(t.kv_hi, t.kv_lo + (k + 1) * size));
-      piece.slot = static_cast<int32_t>(slot++);
-      piece.group = gid;
-      s.decode.push_back(piece);
+  }
+  std::sort(works.begin(), works.end(), std::greater<int64_t>());
+  works.erase(std::unique(works.begin(), works.end()), works.end());
+  auto rank_of = [&](int64_t w) {
+    return static_cast<int32_t>(std::lower_bound(works.begin(), works.end(), w,
+                                                 std::greater<int64_t>()) - works.begin());
+  };
+  struct Ranks {
+    int32_t whole, last;
+  };
+  std::vector<Ranks> rank(nb), late_rank(tail_k > 0 ? nb : 0);
+  for (size_t i = 0; i < nb; ++i) {
+    rank[i] = Ranks{rank_of(whole_work(blocks[i], plan[i])), rank_of(last_work(blocks[i], plan[i]))};
+    if (tail_k > 0)
+      late_rank[i] = Ranks{rank_of(whole_work(blocks[i], late_plan[i])),
+                           rank_of(last_work(blocks[i], late_plan[i]))};
+  }
+  // Late tiles: with tail pieces every tile is whole in the batch rule, so a
+  // tile's place in the longest-first order of whole tiles is the number of
+  // tiles of larger work plus those of its work generated before it.
+  std::vector<int64_t> late_from;  // per work rank: first late index among its tiles
+  if (tail_k > 0) {
+    std::vector<int64_t> count(works.size(), 0);
+    for (size_t i = 0; i < nb; ++i) count[static_cast<size_t>(rank[i].last)] += heads;
+    late_from.resize(works.size());
+    int64_t before = 0;
+    for (size_t r = 0; r < works.size(); ++r) {
+      late_from[r] = std::max<int64_t>(0, slots - before);
+      before += count[r];
     }
+  }
+  // Tiles run in generation order (sequence, KV head, row block). late(i):
+  // whether the next tile of block i is late (`seen` counts the whole tiles
+  // of each work so far).
+  std::vector<int64_t> seen(tail_k > 0 ? works.size() : 0, 0);
+  auto late = [&](size_t i) {
+    if (tail_k == 0) return false;
+    const size_t r = static_cast<size_t>(rank[i].last);
+    return seen[r]++ >= late_from[r];
+  };
+  // Pieces per work, then each piece written to its place.
+  std::vector<int64_t> place(works.size() + 1, 0);
+  int64_t n_pieces = 0, n_groups = 0;
+  auto count = [&](const Cut& c, const Ranks& r, int64_t tiles) {
+    place[static_cast<size_t>(r.whole) + 1] += (c.pieces - 1) * tiles;
+    place[static_cast<size_t>(r.last) + 1] += tiles;
+    n_pieces += c.pieces * tiles;
+    n_groups += c.pieces > 1 ? tiles : 0;
+  };
+  if (tail_k == 0) {
+    for (size_t i = 0; i < nb; ++i) count(plan[i], rank[i], heads);
+  } else {
+    size_t b0 = 0;
+    for (int32_t e : span_end) {
+      for (int32_t g = 0; g < p.num_kv_heads; ++g)
+        for (size_t i = b0; i < static_cast<size_t>(e); ++i)
+          if (late(i)) count(late_plan[i], late_rank[i], 1);
+          else count(plan[i], rank[i], 1);
+      b0 = static_cast<size_t>(e);
+    }
+    std::fill(seen.begin(), seen.end(), 0);
+  }
+  for (size_t r = 0; r < works.size(); ++r) place[r + 1] += place[r];
+  s.decode.resize(static_cast<size_t>(n_pieces));
+  s.groups.resize(static_cast<size_t>(n_groups));
+  ua_tile* const out_tiles = s.decode.data();
+  ua_combine_group* const out_groups = s.groups.data();
+  int64_t* const at = place.data();
+  int32_t slot = 0, gid = 0;
+  size_t b0 = 0;
+  for (int32_t e : span_end) {
+    for (int32_t g = 0; g < p.num_kv_heads; ++g) {
+      for (size_t i = b0; i < static_cast<size_t>(e); ++i) {
+        const bool is_late = late(i);
+        const DecodeBlock& b = blocks[i];
+        const Cut& c = is_late ? late_plan[i] : plan[i];
+        const Ranks& r = is_late ? late_rank[i] : rank[i];
+        ua_tile t;
+        t.seq = b.seq;
+        t.kv_head = g;
+        t.row0 = b.row0;
+        t.nrows = b.nrows;
+        t.kv_lo = b.kv_lo;
+        t.kv_hi = b.kv_hi;
+        t.slot = -1;
+        t.group = -1;
+        if (c.pieces == 1) {
+          out_tiles[at[r.last]++] = t;
+          continue;
+        }
+        ua_combine_group& grp = out_groups[gid];
+        grp.seq = b.seq;
+        grp.kv_head = g;
+        grp.row0 = b.row0;
+        grp.nrows = b.nrows;
+        grp.slot0 = slot;
+        grp.nsplits = static_cast<int32_t>(c.pieces);
+        grp.pad0 = grp.pad1 = 0;
+        t.group = gid++;
+        const int32_t size = static_cast<int32_t>(c.size);
+        for (int64_t k = 0; k + 1 < c.pieces; ++k) {
+          t.kv_hi = t.kv_lo + size;
+          t.slot = slot++;
+          out_tiles[at[r.whole]++] = t;
+          t.kv_lo = t.kv_hi;
+        }
+        t.kv_hi = b.kv_hi;
+        t.slot = slot++;
+        out_tiles[at[r.last]++] = t;
+      }
+    }
+    b0 = static_cast<size_t>(e);
   }
   s.num_slots = slot;
 
-  // 3. Longest work first, so the tail of the grid holds the short tiles;
-  // equal work in (sequence, KV head, row, key) order, the generation order.
-  auto work_of = [](const ua_tile& t) {
-    return static_cast<int64_t>(t.kv_hi - t.kv_lo) * t.nrows;
-  };
-  {
-    const size_t nd = s.decode.size();
-    int64_t max_work = 0;
-    for (const ua_tile& t : s.decode) max_work = std::max(max_work, work_of(t));
-    if (nd < (size_t{1} << 24) && max_work < (int64_t{1} << 39)) {
-      // one 64-bit key per tile: (max_work - work) above a 24-bit index
-      std::vector<uint64_t> keys(nd);
-      for (size_t i = 0; i < nd; ++i)
-        keys[i] = (static_cast<uint64_t>(max_work - work_of(s.decode[i])) << 24) | i;
-      std::sort(keys.begin(), keys.end());
-      std::vector<int32_t> order(nd);
-      for (size_t i = 0; i < nd; ++i) order[i] = static_cast<int32_t>(keys[i] & 0xFFFFFFu);
-      permute(s.decode, order);
-    } else {
-      std::vector<SortKey> keys(nd);
-      for (size_t i = 0; i < nd; ++i)
-        keys[i] = {-work_of(s.decode[i]), 0, 0, static_cast<int32_t>(i)};
-      permute(s.decode, order_by(keys));
-    }
-  }
   // Prefill tiles stay grouped by (sequence, KV head), longest group first and
   // longest tile first inside a group: CTAs running at the same time then read
   // the same K/V rows, which stay in L2 (a head's K/V is a few MB; all heads
   // at once would not fit).
-  {
+  if (!s.prefill.empty()) {
     std::vector<int64_t> group_work(static_cast<size_t>(p.num_seqs) * p.num_kv_heads, 0);
     auto gi = [&](const ua_tile& t) {
       return static_cast<size_t>(t.seq) * p.num_kv_heads + t.kv_head;
@@ -364,10 +508,9 @@ ua_status build_schedule(const Problem& p, Schedule* out) {
     s.prefill_ctas = static_cast<int32_t>(std::min<int64_t>(num_sms, static_cast<int64_t>(n)));
   }
   {
+    // the pieces of a tile cover its keys once: `total` keys in all
     const int elt = p.kv_dtype == UA_KV_FP8_E4M3 ? 1 : 2;
-    int64_t keys = 0;
-    for (const ua_tile& t : s.decode) keys += t.kv_hi - t.kv_lo;
-    s.decode_bytes = keys * 2 * static_cast<int64_t>(p.head_dim) * elt;
+    s.decode_bytes = total * 2 * static_cast<int64_t>(p.head_dim) * elt;
   }
   if (!s.prefill.empty() && !s.decode.empty())
     s.prefill_ctas = mixed_prefill_ctas(s.prefill_blocks, s.decode_bytes,

@@ -358,6 +358,38 @@ def test_nonuniform_decode_keeps_the_average_load_chunk():
     assert max(_piece_lengths(dec)) == chunk
 
 
+def test_short_tiles_overfilling_one_wave_split_only_their_tail():
+    """512 unsplit window tiles (about 1024 keys) on 456 CTA slots: the 56
+    tiles that start last in longest-first order are cut into pieces of at
+    least 256 keys (at most 456 // 56 = 8 each), ordered after every whole
+    tile; the other 456 stay whole. Batches that overfill by more than half a
+    wave keep their tiles whole."""
+    import random
+    rng = random.Random(0)
+    kv = [rng.randint(512, 4096) for _ in range(64)]
+    info, _, dec, grp = _check_schedule(list(range(65)), kv, 32, 8, window=1024)
+    assert info.split_tokens == 0
+    whole = [t for t in dec if t["group"] < 0]
+    pieces = [t for t in dec if t["group"] >= 0]
+    assert len(whole) == 456 and len(grp) == 56
+    assert all(2 <= g["nsplits"] <= 8 for g in grp)
+    assert min(_piece_lengths(pieces)) >= 256 - 16
+    # every piece is scheduled after every whole tile, and the split tiles are
+    # the shortest ones
+    first_piece = min(i for i, t in enumerate(dec) if t["group"] >= 0)
+    assert all(t["group"] < 0 for t in dec[:first_piece]) and first_piece == 456
+    tile_len = {}
+    for t in dec:
+        key = (t["seq"], t["kv_head"])
+        tile_len[key] = tile_len.get(key, 0) + t["kv_hi"] - t["kv_lo"]
+    split = {(g["seq"], g["kv_head"]) for g in grp}
+    assert max(tile_len[k] for k in split) <= min(v for k, v in tile_len.items() if k not in split)
+    # 64 more sequences: 1024 tiles, more than half a wave late -> no split
+    kv2 = kv + kv
+    info, _, dec, grp = _check_schedule(list(range(129)), kv2, 32, 8, window=1024)
+    assert len(grp) == 0 and len(dec) == 1024
+
+
 def test_head_dim_256_splits_for_one_cta_per_sm():
     """At head_dim 256 the decode kernel holds one CTA per SM: uniform pieces
     are sized for 152 slots (whole waves of 152 CTAs)."""

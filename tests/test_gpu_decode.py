@@ -218,6 +218,18 @@ def test_full_size_decode_configs_whole_output(cfg):
     assert_close(got, exp, case.kv_dtype, f"workload {cfg} ({case.name})", report=True)
 
 
+def test_full_size_window_decode_whole_output():
+    """The pure-decode workload with a 1024-key window (the benchmark's
+    `--window 1024` case: its 56 last tiles are cut into tail pieces): every
+    element against the fp64 oracle."""
+    import dataclasses
+    case = dataclasses.replace(W.CONFIGS[2](), window=1024)
+    got = as_f64(tu.run(case))
+    torch.cuda.empty_cache()
+    exp = oracle_full_parallel(case)
+    assert_close(got, exp, case.kv_dtype, f"workload 2, window 1024 ({case.name})", report=True)
+
+
 # ---- head_dim 256 (decode kernel only: V fragments read after the softmax)
 
 @pytest.mark.parametrize("dtype", [W.BF16, W.FP8])
