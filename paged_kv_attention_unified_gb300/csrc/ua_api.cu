@@ -465,6 +465,148 @@ ua_status create_plan(ua_plan** out, const int32_t* cu_query_lens_host,
   return UA_OK;
 }
 
+// ua_forward_host for batches whose query and output copies take about as
+// long as the forward itself: the sequences are cut into kHostChunks
+// contiguous runs of about equal query tokens, each with its own plan, and
+// the copies overlap the compute. Run c goes on `stream` (even c) or a second
+// compute stream (odd c): the copy of its q, its plan upload and its forward,
+// in that order on one stream, so that the next run's q copy overlaps this
+// run's forward and the next run's CTAs fill the SMs this run's last CTAs
+// leave idle. Its output comes back on a copy stream while later runs
+// compute (the host link carries both directions at once). (A q copy on a
+// stream of its own, waited for through an event, held back the forwards
+// until every q had landed.)
+constexpr size_t kHostPipelineMinBytes = size_t{32} << 20;
+constexpr int kHostChunks = 4;
+
+// The internal streams of a device (a compute stream and the output copy
+// stream), created on first use and kept.
+bool host_pipeline_streams(int dev, cudaStream_t (&out)[2]) {
+  static std::mutex mu;
+  static cudaStream_t streams[kMaxDevices][2] = {};
+  if (dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lock(mu);
+  cudaStream_t* st = streams[dev];
+  for (int i = 0; i < 2; ++i) {
+    if (st[i] == nullptr && cudaStreamCreateWithFlags(&st[i], cudaStreamNonBlocking) != cudaSuccess) {
+      st[i] = nullptr;
+      return false;
+    }
+    out[i] = st[i];
+  }
+  return true;
+}
+
+ua_status forward_host_chunked(const void* q_host, void* out_host,
+                               const int32_t* cu_query_lens_host, const int32_t* kv_lens_host,
+                               const int32_t* block_tables_host, const void* k_cache,
+                               const void* v_cache, int32_t num_seqs, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t max_blocks_per_seq, int64_t num_blocks, int32_t kv_dtype,
+                               float scale, int32_t causal, int32_t window, float k_scale,
+                               float v_scale, int32_t num_splits, int32_t* error_word,
+                               ua_stream_t stream) {
+  const int64_t total_q = cu_query_lens_host[num_seqs];
+  const size_t row_bytes = static_cast<size_t>(num_q_heads) * head_dim * 2;
+  const size_t q_bytes = static_cast<size_t>(total_q) * row_bytes;
+  // run c holds sequences [bounds[c], bounds[c + 1])
+  std::vector<int32_t> bounds{0};
+  for (int32_t i = 1; i < num_seqs && static_cast<int>(bounds.size()) < kHostChunks; ++i) {
+    if (static_cast<int64_t>(cu_query_lens_host[i]) * kHostChunks >=
+        static_cast<int64_t>(bounds.size()) * total_q)
+      bounds.push_back(i);
+  }
+  bounds.push_back(num_seqs);
+  const int runs = static_cast<int>(bounds.size()) - 1;
+
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0;
+  cudaStream_t lanes[2];
+  if (cudaGetDevice(&dev) != cudaSuccess || !host_pipeline_streams(dev, lanes))
+    return UA_ERR_CUDA;
+  const cudaStream_t compute[2] = {cs, lanes[0]};
+  const cudaStream_t s_out = lanes[1];
+  // events: [0] buffers allocated, [1 + c] forward of run c done, [1 + runs],
+  // [2 + runs] the side streams drained
+  std::vector<cudaEvent_t> ev(3 + static_cast<size_t>(runs), nullptr);
+  for (cudaEvent_t& e : ev)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      for (cudaEvent_t x : ev)
+        if (x) cudaEventDestroy(x);
+      return UA_ERR_CUDA;
+    }
+  void* dq = nullptr;
+  ua_status st = UA_OK;
+  if (plan_alloc(&dq, 2 * q_bytes, dev, cs) != cudaSuccess) {
+    dq = nullptr;
+    st = UA_ERR_CUDA;
+  }
+  uint8_t* const d_q = static_cast<uint8_t*>(dq);
+  uint8_t* const d_out = d_q + q_bytes;
+  if (st == UA_OK) {
+    st = from_cuda(cudaEventRecord(ev[0], cs));
+    for (cudaStream_t x : {compute[1], s_out})
+      if (st == UA_OK) st = from_cuda(cudaStreamWaitEvent(x, ev[0], 0));
+  }
+  std::vector<ua_plan*> plans(static_cast<size_t>(runs), nullptr);
+  std::vector<int32_t> cu_run;
+  for (int c = 0; c < runs && st == UA_OK; ++c) {
+    const int32_t s0 = bounds[c], n = bounds[c + 1] - bounds[c];
+    const int32_t t0 = cu_query_lens_host[s0];
+    if (cu_query_lens_host[bounds[c + 1]] == t0) continue;  // no query rows in this run
+    const size_t off = static_cast<size_t>(t0) * row_bytes;
+    const size_t bytes = static_cast<size_t>(cu_query_lens_host[bounds[c + 1]] - t0) * row_bytes;
+    const cudaStream_t run_stream = compute[c % 2];
+    st = from_cuda(cudaMemcpyAsync(d_q + off, static_cast<const uint8_t*>(q_host) + off, bytes,
+                                   cudaMemcpyHostToDevice, run_stream));
+    if (st != UA_OK) break;
+    cu_run.resize(static_cast<size_t>(n) + 1);
+    for (int32_t i = 0; i <= n; ++i) cu_run[i] = cu_query_lens_host[s0 + i] - t0;
+    const int32_t* bt = block_tables_host + static_cast<size_t>(s0) * max_blocks_per_seq;
+    const HostRange extra[3] = {
+        {cu_run.data(), (static_cast<size_t>(n) + 1) * sizeof(int32_t)},
+        {kv_lens_host + s0, static_cast<size_t>(n) * sizeof(int32_t)},
+        {bt, static_cast<size_t>(n) * static_cast<size_t>(max_blocks_per_seq) * sizeof(int32_t)}};
+    void* dev_extra[3] = {nullptr, nullptr, nullptr};
+    st = create_plan(&plans[c], cu_run.data(), kv_lens_host + s0, n, num_q_heads, num_kv_heads,
+                     head_dim, block_size, max_blocks_per_seq, kv_dtype, causal, window,
+                     num_splits, -1, reinterpret_cast<ua_stream_t>(run_stream), extra, 3,
+                     dev_extra);
+    if (st != UA_OK) break;
+    st = ua_forward(plans[c], d_q + off, k_cache, v_cache, d_out + off,
+                    static_cast<const int32_t*>(dev_extra[0]),
+                    static_cast<const int32_t*>(dev_extra[1]),
+                    static_cast<const int32_t*>(dev_extra[2]), num_blocks, plans[c]->sched.max_q,
+                    plans[c]->sched.max_kv, scale, k_scale, v_scale,
+                    reinterpret_cast<ua_stream_t>(run_stream));
+    if (st == UA_OK) st = from_cuda(cudaEventRecord(ev[1 + c], run_stream));
+    if (st == UA_OK) st = from_cuda(cudaStreamWaitEvent(s_out, ev[1 + c], 0));
+    if (st == UA_OK)
+      st = from_cuda(cudaMemcpyAsync(static_cast<uint8_t*>(out_host) + off, d_out + off, bytes,
+                                     cudaMemcpyDeviceToHost, s_out));
+  }
+  // Drain the side streams into `stream` (also after a failure), then free.
+  cudaEventRecord(ev[1 + runs], s_out);
+  cudaStreamWaitEvent(cs, ev[1 + runs], 0);
+  cudaEventRecord(ev[2 + runs], compute[1]);
+  cudaStreamWaitEvent(cs, ev[2 + runs], 0);
+  if (dq) cudaFreeAsync(dq, cs);
+  if (cudaStreamSynchronize(cs) != cudaSuccess && st == UA_OK) st = UA_ERR_CUDA;
+  int32_t code = UA_OK;
+  for (ua_plan* pl : plans) {
+    if (pl == nullptr) continue;
+    int32_t v = UA_OK;
+    if (st == UA_OK && code == UA_OK &&
+        cudaMemcpy(&v, pl->d_err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+      st = UA_ERR_CUDA;
+    if (code == UA_OK) code = v;
+    ua_plan_destroy(pl);
+  }
+  if (error_word != nullptr && st == UA_OK) *error_word = code;
+  for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  return st;
+}
+
 }  // namespace
 
 extern "C" {
@@ -731,10 +873,24 @@ ua_status ua_forward_host(const void* q_host, void* out_host, const int32_t* cu_
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const size_t q_bytes =
       static_cast<size_t>(total_q) * static_cast<size_t>(num_q_heads) * head_dim * 2;
+  if (q_bytes > 0 && (!q_host || !out_host)) return UA_ERR_INVALID_ARG;
+  if (q_bytes >= kHostPipelineMinBytes && num_seqs >= 2) {
+    // the scheduler validates the rest per run; check the whole batch first
+    // so that a bad sequence fails the call before any run starts
+    ua::Problem whole = make_problem(cu_query_lens_host, kv_lens_host, num_seqs, num_q_heads,
+                                     num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                     kv_dtype, causal, window, num_splits, 152, -1);
+    const ua_status vs = ua::validate(whole);
+    if (vs != UA_OK) return vs;
+    return forward_host_chunked(q_host, out_host, cu_query_lens_host, kv_lens_host,
+                                block_tables_host, k_cache, v_cache, num_seqs, num_q_heads,
+                                num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                num_blocks, kv_dtype, scale, causal, window, k_scale, v_scale,
+                                num_splits, error_word, stream);
+  }
   void* dq = nullptr;
   int dev = 0;
   if (q_bytes > 0) {
-    if (!q_host || !out_host) return UA_ERR_INVALID_ARG;
     if (cudaGetDevice(&dev) != cudaSuccess) return UA_ERR_CUDA;
     if (plan_alloc(&dq, 2 * q_bytes, dev, cs) != cudaSuccess) return UA_ERR_CUDA;
     if (cudaMemcpyAsync(dq, q_host, q_bytes, cudaMemcpyHostToDevice, cs) != cudaSuccess) {
