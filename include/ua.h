@@ -142,9 +142,14 @@ typedef struct ua_plan ua_plan;
  * Call once with NULL arrays to read the counts into *info, then again with
  * arrays of at least those lengths (the *_cap arguments give their lengths in
  * elements; too small a capacity returns UA_ERR_INVALID_ARG).
- * num_splits: 0 = automatic (enough pieces for num_sms), n > 0 = cut every
- * decode tile's key range into min(n, ceil(len/16)) pieces; at most
- * UA_MAX_SPLITS. num_sms <= 0 means 152.
+ * num_splits: 0 = automatic, n > 0 = cut every decode tile's key range into
+ * min(n, ceil(len/16)) pieces; at most UA_MAX_SPLITS. Automatic: pieces of
+ * about one CTA slot's average load (tiles of nearly one length: unsplit
+ * when a bf16 batch of 256 or more tiles fills one wave of slots, else the
+ * cut that fills whole waves); a batch left unsplit that overfills one wave
+ * by at most half a wave cuts the tiles that start last into pieces of at
+ * least 256 keys (tail pieces), so that they fill the slots the first wave
+ * frees. num_sms <= 0 means 152.
  * decode_rows_max: sequences with q_len * qpk <= this value go to the decode
  * kernel, the others to a prefill kernel (when one takes the problem:
  * head_dim 64, 128, 192 or 256, 128 % qpk == 0, and a bf16 cache whose
