@@ -467,9 +467,17 @@ def measure_attention(cfg, args, rank, world, with_cpu, soak_s, cpu_budget):
         r["timing"] = ("device global-timer span, first CTA start to last CTA end (the two "
                        "kernels of a mixed step overlap), over K steps after the timed ones") \
             if mixed else "CUDA events on the launching stream, over K steps after the timed ones"
+        # records are per launch configuration: options that change what a
+        # launch reads (window, forced splits, CTA count, fp8 products) or its
+        # arithmetic (unified max) look up a key of their own
+        variant = ("f8p" if f8p and kind == "prefill" else "") + \
+            (f"win{args.window}" if args.window else "") + \
+            (f"ns{args.num_splits}" if args.num_splits else "") + \
+            (f"pc{args.prefill_ctas}" if args.prefill_ctas else "") + \
+            ("um" if args.unified_max is not None else "")
         traffic, note, digests = _traffic_record(
             "prefill_wide" if kind == "prefill" and case.head_dim in (192, 256) else kind,
-            f"{cfg}f8p" if f8p and kind == "prefill" else cfg)
+            f"{cfg}{variant}")
         r["traffic"] = traffic
         if note:
             r["traffic_note"] = note
