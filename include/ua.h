@@ -258,15 +258,20 @@ ua_status ua_forward_oneshot(const void* q, const void* k_cache, const void* v_c
  * batch, uploads the tile list together with the lengths and page tables in
  * one copy, copies q to the device, runs the forward, copies the output
  * back, and synchronises `stream` before returning.
- * From 32 MiB of q (and two sequences) the copies would take about as long
- * as the forward, so the batch is cut into up to four runs of consecutive
- * sequences with about equal query tokens, each scheduled on its own. The
- * runs alternate between `stream` and an internal compute stream (each run:
- * copy of its q, plan upload, forward), so that one run's q copy overlaps
- * the previous run's forward, and each output comes back on an internal copy
- * stream while later runs compute. Prefill rows are bit-identical either
- * way; decode rows may differ in rounding, since their split-KV pieces are
- * chosen per run. The whole batch is validated before the first run starts.
+ * From 32 MiB of q the copies would take about as long
+ * as the forward, so the query tokens are cut into runs of about 16 MiB of
+ * q (2 to 4 runs), each scheduled on its own. A cut falls on the first
+ * sequence boundary at or after its target; but inside a sequence at least
+ * a run long, with a causal mask or with neither mask nor window (on a
+ * whole prefill tile, both parts still prefill-sized): rows [a, b) of a
+ * sequence with context ctx run as a sequence of b - a tokens with ctx + b
+ * keys (causal) or all kv_len keys (no mask). The runs alternate between `stream` and an internal compute
+ * stream (each run: copy of its q, plan upload, forward), so that one run's
+ * q copy overlaps the previous run's forward, and each output comes back on
+ * an internal copy stream while later runs compute. Prefill rows are
+ * bit-identical either way; decode rows may differ in rounding, since their
+ * split-KV pieces are chosen per run. The whole batch is validated before
+ * the first run starts.
  * q_host, out_host: [total_q, num_q_heads, head_dim] bf16 in host memory
  *   (page-locked memory, e.g. cudaHostAlloc, gives asynchronous copies;
  *   pageable memory works, its copies synchronise).

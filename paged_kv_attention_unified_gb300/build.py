@@ -58,23 +58,52 @@ _SHARED_SOURCES = ("sm100.cuh", "ua_device.cuh", "ua_kernels.h", "tma_host.cu", 
 
 
 def kernel_digest(kernel: str) -> str:
-    """Digest of the sources one kernel's DRAM traffic depends on (committed
-    ncu traffic records are keyed by it)."""
-    return _digest(only=_KERNEL_SOURCES[kernel] + _SHARED_SOURCES)
+    """Digest of the code one kernel's DRAM traffic depends on (committed ncu
+    traffic records are keyed by it); comments do not count."""
+    return _digest(only=_KERNEL_SOURCES[kernel] + _SHARED_SOURCES, code_only=True)
 
 
-def _digest(extra=(), only=None):
+def _strip_comments(text: str) -> str:
+    """C / C++ source without its comments (string and character literals
+    kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
+def _digest(extra=(), only=None, code_only=False):
     """Hash of the library's sources (by file name, not path) and its compile
     flags with the include paths taken out: the same tree gives the same
-    digest wherever it is checked out. only: restrict to these file names."""
+    digest wherever it is checked out. only: restrict to these file names;
+    code_only: hash the sources without their comments."""
     h = hashlib.sha256()
     files = [(f, CSRC) for f in os.listdir(CSRC)] + [(f, INCLUDE) for f in os.listdir(INCLUDE)]
     for name, base in sorted(files):
         if not name.endswith(_SOURCE_SUFFIXES) or (only is not None and name not in only):
             continue
         with open(os.path.join(base, name), "rb") as fh:
-            h.update(name.encode())
-            h.update(fh.read())
+            data = fh.read()
+        if code_only:
+            data = _strip_comments(data.decode("utf-8")).encode("utf-8")
+        h.update(name.encode())
+        h.update(data)
     h.update(" ".join(f for f in NVCC_FLAGS if not f.startswith("-I")).encode())
     for e in extra:
         h.update(str(e).encode())

@@ -466,18 +466,29 @@ ua_status create_plan(ua_plan** out, const int32_t* cu_query_lens_host,
 }
 
 // ua_forward_host for batches whose query and output copies take about as
-// long as the forward itself: the sequences are cut into kHostChunks
-// contiguous runs of about equal query tokens, each with its own plan, and
-// the copies overlap the compute. Run c goes on `stream` (even c) or a second
-// compute stream (odd c): the copy of its q, its plan upload and its forward,
-// in that order on one stream, so that the next run's q copy overlaps this
-// run's forward and the next run's CTAs fill the SMs this run's last CTAs
-// leave idle. Its output comes back on a copy stream while later runs
-// compute (the host link carries both directions at once). (A q copy on a
-// stream of its own, waited for through an event, held back the forwards
-// until every q had landed.)
+// long as the forward itself: the query tokens are cut into runs of about
+// kHostRunBytes of q each (2 to kHostMaxRuns runs), each with its own plan,
+// and the copies overlap the compute. Run c goes on `stream` (even c) or a
+// second compute stream (odd c): the copy of its q, its plan upload and its
+// forward, in that order on one stream, so that the next run's q copy
+// overlaps this run's forward and the next run's CTAs fill the SMs this
+// run's last CTAs leave idle. Its output comes back on a copy stream while
+// later runs compute (the host link carries both directions at once). (A q
+// copy on a stream of its own, waited for through an event, held back the
+// forwards until every q had landed.)
+// A cut falls on the first sequence boundary at or after its target, unless
+// the sequence holding the target is at least a run long (one long prefill
+// would otherwise be a single run): then, when the mask allows it, the cut
+// falls inside it. With a causal mask, query rows [a, b) of a sequence with
+// context ctx see exactly what a sequence of b - a new tokens and ctx + b
+// keys sees; without a mask or window, what one with all kv_len keys sees.
+// Such cuts fall on whole prefill tiles and leave both parts too long for
+// the decode kernel, so every prefill row takes the same arithmetic as in
+// one plan. (More, shorter runs measured slower: eight runs of half
+// sequences took 1.29 ms per dense-prefill call, four whole ones 1.18 ms.)
 constexpr size_t kHostPipelineMinBytes = size_t{32} << 20;
-constexpr int kHostChunks = 4;
+constexpr size_t kHostRunBytes = size_t{16} << 20;
+constexpr int kHostMaxRuns = 4;
 
 // The internal streams of a device (a compute stream and the output copy
 // stream), created on first use and kept.
@@ -506,18 +517,32 @@ ua_status forward_host_chunked(const void* q_host, void* out_host,
                                float scale, int32_t causal, int32_t window, float k_scale,
                                float v_scale, int32_t num_splits, int32_t* error_word,
                                ua_stream_t stream) {
-  const int64_t total_q = cu_query_lens_host[num_seqs];
+  const int32_t* cu = cu_query_lens_host;
+  const int64_t total_q = cu[num_seqs];
   const size_t row_bytes = static_cast<size_t>(num_q_heads) * head_dim * 2;
   const size_t q_bytes = static_cast<size_t>(total_q) * row_bytes;
-  // run c holds sequences [bounds[c], bounds[c + 1])
-  std::vector<int32_t> bounds{0};
-  for (int32_t i = 1; i < num_seqs && static_cast<int>(bounds.size()) < kHostChunks; ++i) {
-    if (static_cast<int64_t>(cu_query_lens_host[i]) * kHostChunks >=
-        static_cast<int64_t>(bounds.size()) * total_q)
-      bounds.push_back(i);
+  // Run boundaries in query tokens: tok[c] .. tok[c + 1].
+  const int want = static_cast<int>(
+      std::min<size_t>(kHostMaxRuns, std::max<size_t>(2, q_bytes / kHostRunBytes)));
+  const bool cut_inside = causal != 0 || window <= 0;
+  const int64_t qpk = num_q_heads / num_kv_heads;
+  const int64_t align = std::max<int64_t>(1, UA_PREFILL_ROWS / qpk);  // tokens per prefill tile
+  std::vector<int64_t> tok{0};
+  for (int k = 1; k < want; ++k) {
+    const int64_t target = total_q * k / want;
+    // the sequence holding token `target`
+    const int32_t sq = static_cast<int32_t>(std::upper_bound(cu, cu + num_seqs + 1, target) - cu) - 1;
+    const int64_t ql = cu[sq + 1] - cu[sq];
+    const int64_t boundary = cu[sq] == target ? cu[sq] : cu[sq + 1];
+    const int64_t inside = (target - cu[sq]) / align * align;
+    const bool inside_ok = cut_inside && ql * want >= total_q && inside > 0 &&
+                           inside * qpk > ua::kDefaultDecodeRowsMax &&
+                           (ql - inside) * qpk > ua::kDefaultDecodeRowsMax;
+    const int64_t cut = inside_ok ? cu[sq] + inside : boundary;
+    if (cut > tok.back() && cut < total_q) tok.push_back(cut);
   }
-  bounds.push_back(num_seqs);
-  const int runs = static_cast<int>(bounds.size()) - 1;
+  tok.push_back(total_q);
+  const int runs = static_cast<int>(tok.size()) - 1;
 
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   int dev = 0;
@@ -549,26 +574,38 @@ ua_status forward_host_chunked(const void* q_host, void* out_host,
       if (st == UA_OK) st = from_cuda(cudaStreamWaitEvent(x, ev[0], 0));
   }
   std::vector<ua_plan*> plans(static_cast<size_t>(runs), nullptr);
-  std::vector<int32_t> cu_run;
+  std::vector<int32_t> cu_run, kv_run;
   for (int c = 0; c < runs && st == UA_OK; ++c) {
-    const int32_t s0 = bounds[c], n = bounds[c + 1] - bounds[c];
-    const int32_t t0 = cu_query_lens_host[s0];
-    if (cu_query_lens_host[bounds[c + 1]] == t0) continue;  // no query rows in this run
+    const int64_t t0 = tok[c], t1 = tok[c + 1];
+    // sequences s0 .. s0 + n - 1 hold the run's tokens (empty ones between
+    // them included, so that their page-table rows stay consecutive)
+    const int32_t s0 = static_cast<int32_t>(std::upper_bound(cu, cu + num_seqs + 1, t0) - cu) - 1;
+    const int32_t s_last =
+        static_cast<int32_t>(std::upper_bound(cu, cu + num_seqs + 1, t1 - 1) - cu) - 1;
+    const int32_t n = s_last - s0 + 1;
     const size_t off = static_cast<size_t>(t0) * row_bytes;
-    const size_t bytes = static_cast<size_t>(cu_query_lens_host[bounds[c + 1]] - t0) * row_bytes;
+    const size_t bytes = static_cast<size_t>(t1 - t0) * row_bytes;
     const cudaStream_t run_stream = compute[c % 2];
     st = from_cuda(cudaMemcpyAsync(d_q + off, static_cast<const uint8_t*>(q_host) + off, bytes,
                                    cudaMemcpyHostToDevice, run_stream));
     if (st != UA_OK) break;
-    cu_run.resize(static_cast<size_t>(n) + 1);
-    for (int32_t i = 0; i <= n; ++i) cu_run[i] = cu_query_lens_host[s0 + i] - t0;
+    cu_run.assign(1, 0);
+    kv_run.clear();
+    for (int32_t i = s0; i <= s_last; ++i) {
+      const int64_t a = std::max<int64_t>(t0, cu[i]), b = std::min<int64_t>(t1, cu[i + 1]);
+      const int64_t ql = std::max<int64_t>(0, b - a);
+      cu_run.push_back(cu_run.back() + static_cast<int32_t>(ql));
+      // causal: the keys up to the run's last row of this sequence
+      kv_run.push_back(causal != 0 ? static_cast<int32_t>(kv_lens_host[i] - (cu[i + 1] - b))
+                                   : kv_lens_host[i]);
+    }
     const int32_t* bt = block_tables_host + static_cast<size_t>(s0) * max_blocks_per_seq;
     const HostRange extra[3] = {
         {cu_run.data(), (static_cast<size_t>(n) + 1) * sizeof(int32_t)},
-        {kv_lens_host + s0, static_cast<size_t>(n) * sizeof(int32_t)},
+        {kv_run.data(), static_cast<size_t>(n) * sizeof(int32_t)},
         {bt, static_cast<size_t>(n) * static_cast<size_t>(max_blocks_per_seq) * sizeof(int32_t)}};
     void* dev_extra[3] = {nullptr, nullptr, nullptr};
-    st = create_plan(&plans[c], cu_run.data(), kv_lens_host + s0, n, num_q_heads, num_kv_heads,
+    st = create_plan(&plans[c], cu_run.data(), kv_run.data(), n, num_q_heads, num_kv_heads,
                      head_dim, block_size, max_blocks_per_seq, kv_dtype, causal, window,
                      num_splits, -1, reinterpret_cast<ua_stream_t>(run_stream), extra, 3,
                      dev_extra);
@@ -874,7 +911,7 @@ ua_status ua_forward_host(const void* q_host, void* out_host, const int32_t* cu_
   const size_t q_bytes =
       static_cast<size_t>(total_q) * static_cast<size_t>(num_q_heads) * head_dim * 2;
   if (q_bytes > 0 && (!q_host || !out_host)) return UA_ERR_INVALID_ARG;
-  if (q_bytes >= kHostPipelineMinBytes && num_seqs >= 2) {
+  if (q_bytes >= kHostPipelineMinBytes) {
     // the scheduler validates the rest per run; check the whole batch first
     // so that a bad sequence fails the call before any run starts
     ua::Problem whole = make_problem(cu_query_lens_host, kv_lens_host, num_seqs, num_q_heads,

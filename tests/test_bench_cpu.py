@@ -89,3 +89,15 @@ def test_unit_work_adds_up_to_the_whole_forward(window):
     b, f = bench.units_work(case, units)
     tb, tf = bench.algorithmic_work(case)
     assert b == tb - (2 * 3 + 1) * 4 and f == tf
+
+
+def test_kernel_digest_ignores_comments_but_not_code():
+    """The traffic records are keyed by the code of a kernel's sources: a
+    comment edit keeps the digest, a code edit changes it, and comment
+    markers inside string or character literals are code."""
+    from paged_kv_attention_unified_gb300 import build as B
+    src = 'int a = 1; // note\n/* block\n note */ const char* s = "x // y /* z */"; char q = \'"\';'
+    got = B._strip_comments(src)
+    assert "note" not in got and '"x // y /* z */"' in got and "char q = '\"';" in got
+    assert B._strip_comments(src.replace("note", "other words")) == got
+    assert B._strip_comments(src.replace("a = 1", "a = 2")) != got

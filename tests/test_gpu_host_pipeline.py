@@ -38,23 +38,55 @@ def _host_forward(case, b, pinned=True, block_tables=None):
     return err, out_h
 
 
-def _prefill_case():
-    # 6296 query tokens of 32 heads x 128 dims: 51.6 MB of q, two empty
-    # queries between the long ones
-    case = W.make_case("host_runs_prefill", [2048, 0, 2048, 0, 1500, 700],
-                       [2600, 300, 2048, 77, 1900, 700], 32, 8, 128, 16, seed=91)
+def _prefill_case(causal=True, window=0):
+    # 6300 query tokens of 32 heads x 128 dims: 51.6 MB of q in three runs
+    # of 2100 tokens. Both cuts fall in the 5000-token sequence, longer than
+    # a run, so where the mask allows it they fall inside it on whole
+    # prefill tiles (64 tokens of 4-head rows): runs [0, 2048),
+    # [2048, 4160), [4160, 6300), the last holding an empty query too; else
+    # on the next boundary: [0, 5000), [5000, 6300)
+    case = W.make_case("host_runs_prefill", [5000, 0, 1300], [5600, 300, 1300], 32, 8, 128, 16,
+                       seed=91, causal=causal, window=window)
     assert case.q.numel() * 2 >= PIPELINE_MIN_BYTES
     return case
 
 
-@pytest.mark.parametrize("pinned", [True, False])
-def test_runs_of_a_prefill_batch_match_the_planned_path_bit_for_bit(pinned):
-    """Prefill tiles are computed independently of each other, so cutting the
-    batch into runs changes no bit of the output."""
-    case = _prefill_case()
+@pytest.mark.parametrize("causal,window,pinned", [(True, 0, True), (True, 0, False),
+                                                  (False, 0, True), (True, 700, True),
+                                                  (False, 700, True)])
+def test_runs_of_a_prefill_batch_match_the_planned_path_bit_for_bit(causal, window, pinned):
+    """Every row of a prefill tile takes the same arithmetic whatever tiles
+    surround it, and a cut inside a sequence keeps the row positions (causal:
+    the keys up to the run's last row; no mask: all keys; a window without
+    the causal mask cuts only between sequences): the runs change no bit."""
+    case = _prefill_case(causal, window)
     b = tu.to_device(case)
     ref = tu.run(case)
     err, out_h = _host_forward(case, b, pinned)
+    assert err == 0
+    assert torch.equal(out_h.view(torch.int16), ref.view(torch.int16))
+
+
+def test_one_long_prefill_runs_in_pieces_bit_for_bit():
+    """A single causal sequence of 6300 new tokens over 600 tokens of context
+    (51.6 MB of q): three runs of its rows, each over the keys up to its last
+    row, give the one-plan output bit for bit."""
+    case = W.make_case("host_runs_one_seq", [6300], [6900], 32, 8, 128, 16, seed=92)
+    assert case.q.numel() * 2 >= PIPELINE_MIN_BYTES
+    b = tu.to_device(case)
+    ref = tu.run(case)
+    err, out_h = _host_forward(case, b)
+    assert err == 0
+    assert torch.equal(out_h.view(torch.int16), ref.view(torch.int16))
+
+
+def test_runs_of_the_dense_prefill_workload_match_bit_for_bit():
+    """The dense-prefill benchmark workload (4 x 4096 tokens, 134 MB of q in
+    four runs of one sequence each) bit for bit."""
+    case = W.CONFIGS[4]()
+    b = tu.to_device(case)
+    ref = tu.run(case)
+    err, out_h = _host_forward(case, b)
     assert err == 0
     assert torch.equal(out_h.view(torch.int16), ref.view(torch.int16))
 
@@ -79,6 +111,6 @@ def test_a_bad_page_in_the_last_run_is_reported():
     case = _prefill_case()
     b = tu.to_device(case)
     bt = case.block_tables.clone()
-    bt[5, 3] = case.num_blocks + 7          # never dereferenced, reported instead
+    bt[2, 3] = case.num_blocks + 7          # never dereferenced, reported instead
     err, _ = _host_forward(case, b, block_tables=bt)
     assert err == ua.UA_ERR_BOUNDS
