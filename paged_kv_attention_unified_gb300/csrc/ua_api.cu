@@ -950,6 +950,8 @@ ua_status ua_forward_host(const void* q_host, void* out_host, const int32_t* cu_
     if (dq) cudaFreeAsync(dq, cs);
     return st;
   }
+  PinnedBlock word;
+  bool have_word = false;
   if (q_bytes > 0) {
     void* dout = static_cast<uint8_t*>(dq) + q_bytes;
     st = ua_forward(plan, dq, k_cache, v_cache, dout, static_cast<const int32_t*>(dev_extra[0]),
@@ -959,15 +961,25 @@ ua_status ua_forward_host(const void* q_host, void* out_host, const int32_t* cu_
     if (st == UA_OK &&
         cudaMemcpyAsync(out_host, dout, q_bytes, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
       st = UA_ERR_CUDA;
-    if (st == UA_OK && error_word != nullptr &&
-        cudaMemcpyAsync(error_word, plan->d_err, sizeof(int32_t), cudaMemcpyDeviceToHost, cs) !=
-            cudaSuccess)
-      st = UA_ERR_CUDA;
+    // The error word comes back through a pinned block: a copy into the
+    // caller's (usually pageable) word would stage through the driver and
+    // hold the host until the forward is done.
+    if (st == UA_OK && error_word != nullptr) {
+      have_word = pinned_take(sizeof(int32_t), &word);
+      if (cudaMemcpyAsync(have_word ? word.ptr : error_word, plan->d_err, sizeof(int32_t),
+                          cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        st = UA_ERR_CUDA;
+    }
     cudaFreeAsync(dq, cs);
   } else if (error_word != nullptr) {
     *error_word = UA_OK;
   }
   if (cudaStreamSynchronize(cs) != cudaSuccess && st == UA_OK) st = UA_ERR_CUDA;
+  if (have_word) {
+    if (st == UA_OK) *error_word = *static_cast<const int32_t*>(word.ptr);
+    cudaEventRecord(word.done, cs);
+    pinned_give_back(word);
+  }
   ua_plan_destroy(plan);
   return st;
 }

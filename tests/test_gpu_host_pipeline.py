@@ -107,6 +107,22 @@ def test_runs_of_the_mixed_workload_match_the_oracle():
                  f"workload 3 via the host runs ({case.name})", report=True)
 
 
+def test_a_bad_page_is_reported_through_the_one_plan_host_path():
+    """Below the pipelining threshold the error word comes back through a
+    pinned block: a bad page id still reaches the caller's word, and a clean
+    call after it reads UA_OK."""
+    case = W.make_case("host_bad_page_small", [1, 1, 40], [100, 64, 300], 8, 2, 128, 16, seed=93)
+    assert case.q.numel() * 2 < PIPELINE_MIN_BYTES
+    b = tu.to_device(case)
+    bt = case.block_tables.clone()
+    bt[0, 2] = case.num_blocks + 5
+    err, _ = _host_forward(case, b, block_tables=bt)
+    assert err == ua.UA_ERR_BOUNDS
+    err, out_h = _host_forward(case, b)
+    assert err == 0
+    assert torch.equal(out_h.view(torch.int16), tu.run(case).view(torch.int16))
+
+
 def test_a_bad_page_in_the_last_run_is_reported():
     case = _prefill_case()
     b = tu.to_device(case)
