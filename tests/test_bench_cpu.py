@@ -101,3 +101,26 @@ def test_kernel_digest_ignores_comments_but_not_code():
     assert "note" not in got and '"x // y /* z */"' in got and "char q = '\"';" in got
     assert B._strip_comments(src.replace("note", "other words")) == got
     assert B._strip_comments(src.replace("a = 1", "a = 2")) != got
+
+
+def test_traffic_records_belong_to_one_launch_configuration():
+    """A committed ncu record is reported only for the launch configuration
+    it was taken on: a key that no capture wrote (a windowed run, forced
+    splits) yields no traffic, and a record whose digest is not the current
+    code's yields none either."""
+    import json
+    import bench
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        records = json.load(f)
+    assert "decode/workload2win1024" not in records and "decode/workload2ns8" not in records
+    assert bench._traffic_record("decode", "2win1024")[0] is None
+    assert bench._traffic_record("decode", "2ns8")[0] is None
+    for key, rec in records.items():
+        if key.startswith("_"):
+            continue
+        kernel, cfg = key.split("/")
+        got, _, digests = bench._traffic_record(kernel, cfg[len("workload"):])
+        if digests["current"] == rec["source_hash"]:
+            assert got == rec["bytes_per_launch"]
+        else:
+            assert got is None
