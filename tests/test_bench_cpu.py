@@ -112,9 +112,12 @@ def test_traffic_records_belong_to_one_launch_configuration():
     import bench
     with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
         records = json.load(f)
-    assert "decode/workload2win1024" not in records and "decode/workload2ns8" not in records
-    assert bench._traffic_record("decode", "2win1024")[0] is None
+    assert "decode/workload2ns8" not in records and "decode/workload2win512" not in records
     assert bench._traffic_record("decode", "2ns8")[0] is None
+    assert bench._traffic_record("decode", "2win512")[0] is None
+    if "decode/workload2win1024" in records and "decode/workload2" in records:
+        assert records["decode/workload2win1024"]["bytes_per_launch"] < \
+            records["decode/workload2"]["bytes_per_launch"] / 2   # the window reads 41 % of the cache
     for key, rec in records.items():
         if key.startswith("_"):
             continue
